@@ -1,0 +1,242 @@
+// C-ABI entry points of libxs (declared in include/xs.h): argument validation,
+// TMA tensor-map encoding and kernel launches. Host code only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/xs.h"
+#include "internal.h"
+
+#define XS_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  static std::mutex mu;
+  static int cached[64] = {0};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return -1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validation shared by every entry point, in the order the header states.
+xs_status validate(const void *const *ptrs, int nptrs, void *const *shards, int B, int N, int H,
+                   int d, int P, int store_tile) {
+  for (int i = 0; i < nptrs; ++i)
+    if (!ptrs[i]) return XS_ERR_INVALID;
+  if (B < 0 || N < 0 || H < 0) return XS_ERR_INVALID;
+  if (shards) {
+    if (P < 1 || P > xs::kMaxShards) return XS_ERR_INVALID;
+    for (int p = 0; p < P; ++p)
+      if (!shards[p]) return XS_ERR_INVALID;
+    if (N % P != 0) return XS_ERR_INVALID;
+  }
+  if (store_tile != 1 && store_tile != 2 && store_tile != 4 && store_tile != 8)
+    return XS_ERR_INVALID;
+  if (d != 64 && d != 128) return XS_ERR_UNSUPPORTED;
+  if (N % xs::kTileRows != 0) return XS_ERR_UNSUPPORTED;
+  for (int i = 0; i < nptrs; ++i)
+    if (!aligned16(ptrs[i])) return XS_ERR_ALIGN;
+  if (shards)
+    for (int p = 0; p < P; ++p)
+      if (!aligned16(shards[p])) return XS_ERR_ALIGN;
+  return XS_OK;
+}
+
+bool encode(CUtensorMap *m, void *base, int rank, const cuuint64_t *dims,
+            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), base, dims,
+            strides_bytes, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q/k/v: 3-D {d, N, B*H}, box {64, 128, 1}.
+bool encode_qkv(CUtensorMap *m, const void *base, int B, int N, int H, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(B) * H};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(xs::kTileRows), 1};
+  return encode(m, const_cast<void *>(base), 3, dims, strides, box);
+}
+
+// Destination rows: 2-D {cols, rows}, row pitch cols*2 bytes, box {64, 16}.
+bool encode_rows(CUtensorMap *m, void *base, unsigned long long cols, unsigned long long rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(xs::kSlabRows)};
+  return encode(m, base, 2, dims, strides, box);
+}
+
+xs_status launch_attention(const void *q, const void *k, const void *v, void *o,
+                           void *const *shards, int B, int N, int H, int d, int P, int store_tile,
+                           cudaStream_t stream) {
+  xs::AttnParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  if (!encode_qkv(&prm.tm_q, q, B, N, H, d) || !encode_qkv(&prm.tm_k, k, B, N, H, d) ||
+      !encode_qkv(&prm.tm_v, v, B, N, H, d))
+    return XS_ERR_CUDA;
+  if (shards) {
+    const int R = N / P;
+    for (int p = 0; p < P; ++p)
+      if (!encode_rows(&prm.tm_out[p], shards[p], static_cast<unsigned long long>(H) * d,
+                       static_cast<unsigned long long>(B) * R))
+        return XS_ERR_CUDA;
+    prm.shard_mode = 1;
+    prm.rows_per_shard = R;
+    prm.P = P;
+  } else {
+    if (!encode_rows(&prm.tm_out[0], o, static_cast<unsigned long long>(d),
+                     static_cast<unsigned long long>(B) * H * N))
+      return XS_ERR_CUDA;
+    prm.shard_mode = 0;
+    prm.rows_per_shard = N;
+    prm.P = 1;
+  }
+  prm.B = B;
+  prm.N = N;
+  prm.H = H;
+  prm.store_tile = store_tile;
+  prm.n_qtiles = N / xs::kTileRows;
+  prm.n_pairs = (prm.n_qtiles + 1) / 2;
+  prm.n_units = B * H * prm.n_pairs;
+  prm.n_kv = N / xs::kTileRows;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  prm.wait_limit_ns = g_wait_limit_ns.load();
+  const int sms = sm_count();
+  if (sms <= 0) return XS_ERR_CUDA;
+  const int grid = prm.n_units < sms ? prm.n_units : sms;
+  return xs::launch_attn(prm, d, grid, stream) == cudaSuccess ? XS_OK : XS_ERR_CUDA;
+}
+
+xs_status launch_layout(const void *o, void *const *shards, int B, int N, int H, int d, int P,
+                        cudaStream_t stream) {
+  xs::ShardPtrs sh;
+  for (int p = 0; p < xs::kMaxShards; ++p) sh.p[p] = p < P ? shards[p] : nullptr;
+  const int sms = sm_count();
+  if (sms <= 0) return XS_ERR_CUDA;
+  const long long vectors = static_cast<long long>(B) * H * N * (d / 8);
+  long long grid = (vectors + 255) / 256;
+  if (grid > static_cast<long long>(sms) * 8) grid = static_cast<long long>(sms) * 8;
+  if (grid < 1) grid = 1;
+  return xs::launch_scatter(o, sh, B, N, H, d, N / P, static_cast<int>(grid), stream) == cudaSuccess
+             ? XS_OK
+             : XS_ERR_CUDA;
+}
+
+bool empty(int B, int N, int H) { return B == 0 || N == 0 || H == 0; }
+
+}  // namespace
+
+XS_API xs_status xs_attn_fused(const void *q, const void *k, const void *v,
+                               void *const *out_shards, int B, int N, int H, int d, int P,
+                               int store_tile, void *stream) {
+  if (!out_shards) return XS_ERR_INVALID;
+  const void *ptrs[3] = {q, k, v};
+  xs_status st = validate(ptrs, 3, out_shards, B, N, H, d, P, store_tile);
+  if (st != XS_OK || empty(B, N, H)) return st;
+  return launch_attention(q, k, v, nullptr, out_shards, B, N, H, d, P, store_tile,
+                          static_cast<cudaStream_t>(stream));
+}
+
+XS_API xs_status xs_attn(const void *q, const void *k, const void *v, void *o, int B, int N, int H,
+                         int d, void *stream) {
+  const void *ptrs[4] = {q, k, v, o};
+  xs_status st = validate(ptrs, 4, nullptr, B, N, H, d, 1, 8);
+  if (st != XS_OK || empty(B, N, H)) return st;
+  return launch_attention(q, k, v, o, nullptr, B, N, H, d, 1, 8,
+                          static_cast<cudaStream_t>(stream));
+}
+
+XS_API xs_status xs_scatter(const void *o, void *const *out_shards, int B, int N, int H, int d,
+                            int P, void *stream) {
+  if (!out_shards) return XS_ERR_INVALID;
+  const void *ptrs[1] = {o};
+  xs_status st = validate(ptrs, 1, out_shards, B, N, H, d, P, 8);
+  if (st != XS_OK || empty(B, N, H)) return st;
+  return launch_layout(o, out_shards, B, N, H, d, P, static_cast<cudaStream_t>(stream));
+}
+
+XS_API xs_status xs_attn_serial(const void *q, const void *k, const void *v, void *o_scratch,
+                                void *const *out_shards, int B, int N, int H, int d, int P,
+                                void *stream) {
+  if (!out_shards) return XS_ERR_INVALID;
+  const void *ptrs[4] = {q, k, v, o_scratch};
+  xs_status st = validate(ptrs, 4, out_shards, B, N, H, d, P, 8);
+  if (st != XS_OK || empty(B, N, H)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_attention(q, k, v, o_scratch, nullptr, B, N, H, d, 1, 8, s);
+  if (st != XS_OK) return st;
+  return launch_layout(o_scratch, out_shards, B, N, H, d, P, s);
+}
+
+XS_API const char *xs_status_string(xs_status s) {
+  switch (s) {
+    case XS_OK: return "ok";
+    case XS_ERR_INVALID: return "invalid argument";
+    case XS_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, N a multiple of 128)";
+    case XS_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case XS_ERR_CUDA: return "CUDA error";
+    case XS_ERR_TIMEOUT: return "on-chip wait timed out";
+  }
+  return "unknown status";
+}
+
+XS_API xs_status xs_last_device_status(void *stream) {
+  int v = 0;
+  if (xs::read_and_clear_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess)
+    return XS_ERR_CUDA;
+  return v == xs::kDevTimeout ? XS_ERR_TIMEOUT : (v == 0 ? XS_OK : XS_ERR_CUDA);
+}
+
+XS_API unsigned long long xs_set_wait_limit_ns(unsigned long long limit_ns) {
+  return g_wait_limit_ns.exchange(limit_ns ? limit_ns : kDefaultWaitLimitNs);
+}
+
+XS_API xs_status xs_selftest_bounded_wait(void *stream) {
+  return xs::launch_wait_selftest(g_wait_limit_ns.load(), static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? XS_OK
+             : XS_ERR_CUDA;
+}
+
+XS_API int xs_abi_version(void) { return 1; }

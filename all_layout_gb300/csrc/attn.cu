@@ -1,0 +1,544 @@
+// Non-causal attention fused with the post-attention Ulysses All-to-All layout,
+// for sm_103a (tcgen05 tensor cores, Tensor Memory, TMA).
+//
+// Method: "X-Stage: An Overlooked Pipeline Stage for Communication-Computation
+// Overlap in DiT Inference". Abstract: tile-granular fusion of the post-attention
+// All-to-All with FlashAttention, where the owner of an output tile issues the
+// tile's stores itself and resumes computation, without a dedicated
+// communication warp or SM. Figure 6: FlashAttention Q-loop and output tiling.
+// Figure 7 / Figure 1: the stores of one tile drain while the next mainloop
+// computes. Pith review, "If this is right": a Q-loop longer than the recovery
+// gap absorbs the drain.
+//
+// Work unit: one (batch, head) and a PAIR of 128-row query tiles. A persistent
+// CTA walks units head-major, so a head's K/V stay hot in L2 across CTAs.
+//
+// Roles (320 threads, one CTA per SM):
+//   warps 0-3  softmax warp group 0: owns query tile 0 of the unit (S0, P0, O0)
+//   warps 4-7  softmax warp group 1: owns query tile 1 (S1, P1, O1)
+//   warp 8     MMA issuer (one thread) + Tensor Memory allocation
+//   warp 9     TMA loader (one thread)
+// Each softmax warp group also rescales its O rows, finalises them, stages the
+// bf16 tile in shared memory and issues the tile's stores to the destination
+// shards as TMA bulk stores, store_tile 16-row slabs after each KV iteration of
+// its next unit. No warp exists only to store.
+//
+// Tensor Memory (512 columns x 128 lanes, row r of a tile = lane r):
+//   S0 [0,128)  S1 [128,256)  O0 [256,256+d)  O1 [256+d,256+2d)
+//   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
+// Shared memory (d = 128): Q0 Q1 | 3 K/V slots | 2 output staging tiles | barriers,
+// every tile stored as 64-column halves of 128 rows x 128 bytes, 128-byte swizzle.
+//
+// MMA order per KV step j (t = 0, 1):  O_t += P_t(j-1) V(j-1);  S_t = Q_t K(j)^T.
+// tcgen05 operations issued by one thread execute in order, so S_t(j) cannot
+// overwrite P_t(j-1) before the PV MMA that reads it; and the commit that
+// signals S_t(j) also covers PV_t(j-1), so the softmax group may rescale O_t as
+// soon as it sees S_t(j).
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace xs {
+
+__device__ int g_status;
+
+namespace {
+
+constexpr int BM = kTileRows;            // query rows per tile
+constexpr int BN = kTileRows;            // keys per KV tile
+constexpr int NSLAB = BM / kSlabRows;    // 8 slabs per output tile
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kHalfBytes = BM * 128;     // one 64-column half of a 128-row tile
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int NH = D / 64;
+  static constexpr int TILE = BM * D * 2;
+  static constexpr int KV_STAGES = (D == 128) ? 3 : 6;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + 2 * TILE;
+  static constexpr int OFF_STG = OFF_KV + KV_STAGES * TILE;
+  static constexpr int OFF_BAR = OFF_STG + 2 * TILE;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
+  static constexpr uint32_t COL_O0 = 256, COL_O1 = 256 + D;
+};
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[6], kv_empty[6];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t wg_sync[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block too large");
+
+__device__ __forceinline__ void record_timeout(volatile int *abort_flag) {
+  *abort_flag = 1;
+  atomicExch(&g_status, kDevTimeout);
+}
+
+// Bounded wait on a barrier phase. Gives up when another role has aborted or
+// when `limit` ns pass, in which case it records a timeout.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                        uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit) {
+        record_timeout(abort_flag);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while tearing down after an abort: ignores the abort flag, still bounded.
+__device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// ------------------------------------------------------------------ TMA loader
+template <int D>
+__device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volatile int *abort_flag) {
+  using C = Cfg<D>;
+  const uint64_t lim = p.wait_limit_ns;
+  uint32_t it = 0;          // K/V slot uses so far (K and V each take one)
+  uint32_t q_armed = 0;     // q_full phases armed so far
+  uint32_t lu = 0;          // units processed by this CTA
+  const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
+    const int bh = u / p.n_pairs, pair = u % p.n_pairs;
+    const int q0a = pair * 2 * BM;
+    const int q0b = (2 * pair + 1 < p.n_qtiles) ? q0a + BM : q0a;  // missing tile: reload tile 0
+    if (lu > 0 && !wait_phase(q_empty, (lu - 1) & 1, abort_flag, lim)) goto drain;
+    mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+    ++q_armed;
+    for (int hf = 0; hf < C::NH; ++hf) {
+      tma_load_3d(smem_u32(smem + C::OFF_Q + hf * kHalfBytes), &p.tm_q, q_full, hf * 64, q0a, bh);
+      tma_load_3d(smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), &p.tm_q, q_full, hf * 64,
+                  q0b, bh);
+    }
+    for (int j = 0; j < p.n_kv; ++j) {
+      for (int kind = 0; kind < 2; ++kind, ++it) {
+        const uint32_t slot = it % C::KV_STAGES, ph = (it / C::KV_STAGES) & 1;
+        if (!wait_phase(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) goto drain;
+        const uint32_t full = smem_u32(&bars->kv_full[slot]);
+        mbar_arrive_expect_tx(full, C::TILE);
+        const CUtensorMap *m = kind == 0 ? &p.tm_k : &p.tm_v;
+        for (int hf = 0; hf < C::NH; ++hf)
+          tma_load_3d(smem_u32(smem + C::OFF_KV + slot * C::TILE + hf * kHalfBytes), m, full,
+                      hf * 64, j * BN, bh);
+      }
+    }
+  }
+drain:
+  // Every load this thread issued must land before the CTA releases its smem:
+  // wait for the most recently armed phase of each barrier it armed.
+  for (uint32_t s = 0; s < (uint32_t)C::KV_STAGES && s < it; ++s) {
+    const uint32_t last = s + ((it - 1 - s) / C::KV_STAGES) * C::KV_STAGES;  // last use of slot s
+    drain_phase(smem_u32(&bars->kv_full[s]), (last / C::KV_STAGES) & 1, lim);
+  }
+  if (q_armed > 0) drain_phase(q_full, (q_armed - 1) & 1, lim);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int D>
+__device__ __forceinline__ void issue_qk(uint8_t *smem, uint32_t tmem, int t, uint32_t slot) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0);
+  const uint32_t qb = smem_u32(smem + C::OFF_Q + t * C::TILE);
+  const uint32_t kb = smem_u32(smem + C::OFF_KV + slot * C::TILE);
+  const uint32_t dcol = tmem + (t == 0 ? C::COL_S0 : C::COL_S1);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * kHalfBytes + (kk % 4) * 32;
+    tc_mma_ss(dcol, smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idesc,
+              kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint8_t *smem, uint32_t tmem, int t, uint32_t slot,
+                                         uint32_t accumulate) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, 1);
+  const uint32_t vb = smem_u32(smem + C::OFF_KV + slot * C::TILE);
+  const uint32_t pcol = tmem + (t == 0 ? C::COL_S0 : C::COL_S1);
+  const uint32_t dcol = tmem + (t == 0 ? C::COL_O0 : C::COL_O1);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    // V is the MN-major B operand: 16 key rows per MMA (2 KiB of the swizzled
+    // tile), the next 64 columns of d one half (kHalfBytes) further.
+    tc_mma_ts(dcol, pcol + kk * 8, smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idesc,
+              (kk > 0 || accumulate) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem,
+                         volatile int *abort_flag) {
+  using C = Cfg<D>;
+  const uint64_t lim = p.wait_limit_ns;
+  uint32_t it = 0, lu = 0;
+  uint32_t pc[2] = {0, 0};
+  const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
+  auto kv_full = [&](uint32_t s) { return smem_u32(&bars->kv_full[s]); };
+  auto kv_empty = [&](uint32_t s) { return smem_u32(&bars->kv_empty[s]); };
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
+    if (!wait_phase(q_full, lu & 1, abort_flag, lim)) goto drain;
+    {
+      const uint32_t sk = it % C::KV_STAGES;
+      if (!wait_phase(kv_full(sk), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t) {
+        issue_qk<D>(smem, tmem, t, sk);
+        tc_commit(smem_u32(&bars->s_full[t]));
+      }
+      tc_commit(kv_empty(sk));
+      ++it;
+      if (p.n_kv == 1) tc_commit(q_empty);
+    }
+    for (int j = 1; j < p.n_kv; ++j) {
+      const uint32_t sv = it % C::KV_STAGES, sk = (it + 1) % C::KV_STAGES;
+      if (!wait_phase(kv_full(sv), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
+      if (!wait_phase(kv_full(sk), ((it + 1) / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
+      for (int t = 0; t < 2; ++t) {
+        if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
+        ++pc[t];
+        tc_fence_after();
+        issue_pv<D>(smem, tmem, t, sv, j > 1 ? 1u : 0u);
+        issue_qk<D>(smem, tmem, t, sk);
+        tc_commit(smem_u32(&bars->s_full[t]));
+      }
+      tc_commit(kv_empty(sv));
+      tc_commit(kv_empty(sk));
+      it += 2;
+      if (j == p.n_kv - 1) tc_commit(q_empty);
+    }
+    {
+      const uint32_t sv = it % C::KV_STAGES;
+      if (!wait_phase(kv_full(sv), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
+      for (int t = 0; t < 2; ++t) {
+        if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
+        ++pc[t];
+        tc_fence_after();
+        issue_pv<D>(smem, tmem, t, sv, p.n_kv > 1 ? 1u : 0u);
+        tc_commit(smem_u32(&bars->o_full[t]));
+      }
+      tc_commit(kv_empty(sv));
+      ++it;
+    }
+  }
+drain:
+  // All MMAs this thread issued must finish before Tensor Memory is released.
+  tc_commit(smem_u32(&bars->drain));
+  drain_phase(smem_u32(&bars->drain), 0, lim);
+}
+
+// ------------------------------------------------------------------ softmax / epilogue
+template <int D>
+struct StoreState {
+  int bh, q0, next;   // pending tile and the next slab to issue (NSLAB: nothing pending)
+};
+
+template <int D>
+__device__ __forceinline__ void issue_slabs(const AttnParams &p, const uint8_t *stg,
+                                            StoreState<D> &ss, int count) {
+  using C = Cfg<D>;
+  int issued = 0;
+  while (ss.next < NSLAB && issued < count) {
+    const int s = ss.next;
+    const int n0 = ss.q0 + s * kSlabRows;
+    const CUtensorMap *m;
+    int x0, y;
+    if (p.shard_mode == 0) {
+      m = &p.tm_out[0];
+      x0 = 0;
+      y = ss.bh * p.N + n0;
+    } else {
+      const int b = ss.bh / p.H, h = ss.bh - b * p.H;
+      const int sh = n0 / p.rows_per_shard;   // a 16-row slab never straddles two shards
+      const int i0 = n0 - sh * p.rows_per_shard;
+      m = &p.tm_out[sh];
+      x0 = h * D;
+      y = b * p.rows_per_shard + i0;
+    }
+#pragma unroll
+    for (int hf = 0; hf < C::NH; ++hf)
+      tma_store_2d(m, smem_u32(stg + (s * C::NH + hf) * (kSlabRows * 128)), x0 + hf * 64, y);
+    ++ss.next;
+    ++issued;
+  }
+  if (issued) bulk_commit();
+}
+
+template <int D>
+__device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem,
+                             volatile int *abort_flag) {
+  using C = Cfg<D>;
+  const uint64_t lim = p.wait_limit_ns;
+  const int t = threadIdx.x / 128;          // warp group = query tile of the unit
+  const int wq = (threadIdx.x / 32) & 3;    // warp within the group = TMEM lane quarter
+  const int lane = threadIdx.x & 31;
+  const int row = wq * 32 + lane;           // tile row owned by this thread
+  const bool elected = (threadIdx.x & 127) == 0;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_base + (t == 0 ? C::COL_S0 : C::COL_S1);
+  const uint32_t tO = tmem + lane_base + (t == 0 ? C::COL_O0 : C::COL_O1);
+  const uint32_t s_full = smem_u32(&bars->s_full[t]), p_full = smem_u32(&bars->p_full[t]);
+  const uint32_t o_full = smem_u32(&bars->o_full[t]), wg_sync = smem_u32(&bars->wg_sync[t]);
+  uint8_t *stg = smem + C::OFF_STG + t * C::TILE;
+  const float scale = p.scale_log2;
+  uint32_t sc = 0, wgc = 0, lu = 0;
+  StoreState<D> ss{0, 0, NSLAB};
+
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
+    const int bh = u / p.n_pairs, pair = u % p.n_pairs;
+    const int qtile = 2 * pair + t;
+    const bool active = qtile < p.n_qtiles;
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < p.n_kv; ++j) {
+      bool ok = wait_phase(s_full, sc & 1, abort_flag, lim);
+      ++sc;
+      if (!__all_sync(0xffffffffu, ok)) goto teardown;
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
+      tmem_wait_ld();
+      float mx = __uint_as_float(s[0][0]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
+      const float m_new = fmaxf(m, mx * scale);
+      // Conditional rescale: keep the running max unless it grew by more than
+      // 2^kRescaleThreshold, so O is rescaled only on the rare large jumps.
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {
+        m = m_new;
+      } else {
+        const bool need = m_new > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          rescale = true;
+          if (need) {
+            alpha = ex2_approx(m - m_new);
+            m = m_new;
+          }
+        }
+      }
+      l *= alpha;
+      const float neg_m = -m;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i]), scale, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i + 1]), scale, neg_m));
+          l += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the S columns already read
+      }
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      // Burst shaping: the previous tile's stores ride on this KV iteration.
+      if (elected && ss.next < NSLAB) issue_slabs<D>(p, stg, ss, p.store_tile);
+    }
+    {
+      // Epilogue: O_t is final once the last PV MMA completes.
+      bool ok = wait_phase(o_full, lu & 1, abort_flag, lim);
+      if (!__all_sync(0xffffffffu, ok)) goto teardown;
+      tc_fence_after();
+      if (elected) {
+        issue_slabs<D>(p, stg, ss, NSLAB);   // leftovers of the previous tile
+        bulk_wait_read_all();                // staging buffer may be overwritten now
+      }
+      mbar_arrive(wg_sync);
+      ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
+      ++wgc;
+      if (!__all_sync(0xffffffffu, ok)) goto teardown;
+      if (active) {
+        const float inv_l = 1.f / l;
+        const int slab = row / kSlabRows, r16 = row % kSlabRows;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+          const int hf = (32 * c) / 64;
+          uint8_t *box = stg + (slab * C::NH + hf) * (kSlabRows * 128) + r16 * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int chunk = ((32 * c) % 64) / 8 + k;   // 16-byte chunk within the 128-byte row
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+            *reinterpret_cast<uint4 *>(box + ((chunk ^ (r16 & 7)) * 16)) = v;
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(wg_sync);
+      ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
+      ++wgc;
+      if (!__all_sync(0xffffffffu, ok)) goto teardown;
+      if (active) ss = StoreState<D>{bh, qtile * BM, 0};
+    }
+  }
+  if (elected) issue_slabs<D>(p, stg, ss, NSLAB);
+teardown:
+  if (elected) bulk_wait_all();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
+  volatile int *abort_flag = &bars->abort;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->q_full), 1);
+    mbar_init(smem_u32(&bars->q_empty), 1);
+    for (int s = 0; s < C::KV_STAGES; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bars->s_full[t]), 1);
+      mbar_init(smem_u32(&bars->p_full[t]), 128);
+      mbar_init(smem_u32(&bars->o_full[t]), 1);
+      mbar_init(smem_u32(&bars->wg_sync[t]), 128);
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) load_role<D>(p, smem, bars, abort_flag);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_role<D>(p, smem, bars, tmem, abort_flag);
+    __syncwarp();
+  } else {
+    softmax_role<D>(p, smem, bars, tmem, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on `bar`: the wait must run out and record a timeout.
+    wait_phase(smem_u32(&bar), 0, &abort_flag, limit_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+int attn_smem_bytes(int d) { return d == 128 ? Cfg<128>::SMEM : Cfg<64>::SMEM; }
+
+cudaError_t launch_attn(const AttnParams &p, int d, int grid, cudaStream_t s) {
+  cudaError_t e;
+  if (d == 128) {
+    e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<128>::SMEM);
+    if (e != cudaSuccess) return e;
+    attn_kernel<128><<<grid, kThreads, Cfg<128>::SMEM, s>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<64>::SMEM);
+    if (e != cudaSuccess) return e;
+    attn_kernel<64><<<grid, kThreads, Cfg<64>::SMEM, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(cudaStream_t s, int *out) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return cudaSuccess;
+}
+
+}  // namespace xs

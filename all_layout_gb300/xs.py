@@ -1,0 +1,150 @@
+"""ctypes binding of libxs (include/xs.h): argument marshalling only.
+
+Every step of the hot path runs in the library's CUDA kernels; this module
+turns torch CUDA tensors into device pointers and a stream handle and raises
+``XsError`` on a non-OK status. Importing it loads ``libxs.so`` and fails
+loudly if the library has not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libxs.so")
+_HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "include", "xs.h")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT = range(6)
+MAX_SHARDS = 8
+
+
+class XsError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libxs.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_vp, _i = ctypes.c_void_p, ctypes.c_int
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_lib.xs_attn_fused.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _i, _vp]
+_lib.xs_attn.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+_lib.xs_scatter.argtypes = [_vp, _PP, _i, _i, _i, _i, _i, _vp]
+_lib.xs_attn_serial.argtypes = [_vp, _vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
+for _f in ("xs_attn_fused", "xs_attn", "xs_scatter", "xs_attn_serial",
+           "xs_last_device_status", "xs_selftest_bounded_wait"):
+    getattr(_lib, _f).restype = _i
+_lib.xs_status_string.argtypes = [_i]
+_lib.xs_status_string.restype = ctypes.c_char_p
+_lib.xs_last_device_status.argtypes = [_vp]
+_lib.xs_selftest_bounded_wait.argtypes = [_vp]
+_lib.xs_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+_lib.xs_set_wait_limit_ns.restype = ctypes.c_ulonglong
+_lib.xs_abi_version.restype = _i
+
+
+def library():
+    """The loaded ctypes library (for direct C-ABI calls)."""
+    return _lib
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def declared_symbols():
+    """Function names declared in include/xs.h."""
+    text = open(_HEADER).read()
+    return sorted(set(re.findall(r"\b(xs_[a-z_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return _lib.xs_status_string(int(status)).decode()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _shard_array(shards):
+    arr = (ctypes.c_void_p * max(1, len(shards)))()
+    for i, s in enumerate(shards):
+        arr[i] = s if isinstance(s, int) else (s.data_ptr() if s is not None else None)
+    return ctypes.cast(arr, _PP), arr
+
+
+def _check(status, what):
+    if status != OK:
+        raise XsError(status, what)
+
+
+def _dims(q):
+    B, H, N, d = q.shape
+    return int(B), int(N), int(H), int(d)
+
+
+def attn_fused(q, k, v, shards, store_tile: int = 8, stream=None):
+    """Fused attention + shard layout. q, k, v: [B, H, N, d] bf16 CUDA tensors;
+    shards: P tensors [B, N/P, H, d] bf16."""
+    B, N, H, d = _dims(q)
+    pp, keep = _shard_array(shards)
+    _check(_lib.xs_attn_fused(_ptr(q), _ptr(k), _ptr(v), pp, B, N, H, d, len(shards),
+                              int(store_tile), _stream(stream)), "xs_attn_fused")
+
+
+def attn(q, k, v, o, stream=None):
+    """Attention alone into o [B, H, N, d] bf16."""
+    B, N, H, d = _dims(q)
+    _check(_lib.xs_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, N, H, d, _stream(stream)),
+           "xs_attn")
+
+
+def scatter(o, shards, stream=None):
+    """Layout alone: o [B, H, N, d] -> shards."""
+    B, N, H, d = _dims(o)
+    pp, keep = _shard_array(shards)
+    _check(_lib.xs_scatter(_ptr(o), pp, B, N, H, d, len(shards), _stream(stream)), "xs_scatter")
+
+
+def attn_serial(q, k, v, o_scratch, shards, stream=None):
+    """Serial execution: attention into o_scratch, then the layout kernel."""
+    B, N, H, d = _dims(q)
+    pp, keep = _shard_array(shards)
+    _check(_lib.xs_attn_serial(_ptr(q), _ptr(k), _ptr(v), _ptr(o_scratch), pp, B, N, H, d,
+                               len(shards), _stream(stream)), "xs_attn_serial")
+
+
+def last_device_status(stream=None) -> int:
+    return int(_lib.xs_last_device_status(_stream(stream)))
+
+
+def set_wait_limit_ns(limit_ns: int) -> int:
+    return int(_lib.xs_set_wait_limit_ns(int(limit_ns)))
+
+
+def selftest_bounded_wait(stream=None):
+    _check(_lib.xs_selftest_bounded_wait(_stream(stream)), "xs_selftest_bounded_wait")
+
+
+def alloc_shards(B, N, H, d, P, device="cuda"):
+    """P separate destination buffers [B, N/P, H, d] bf16 (one allocation each)."""
+    return [torch.empty((B, N // P, H, d), dtype=torch.bfloat16, device=device)
+            for _ in range(P)]

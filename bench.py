@@ -1,0 +1,375 @@
+"""Benchmark: fused non-causal attention + Ulysses post-attention All-to-All layout.
+
+One step = one xs_attn_fused call over one batch of synthetic input already
+resident in HBM (the whole hot path: attention plus the shard stores).
+Metric: attention TFLOP/s = 4*B*N^2*H*d / t, with % of the measured bf16 peak,
+plus fused vs serial (attention then the layout kernel) and attention-alone
+times on the same GPU.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl xs|reference]
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(the (batch, head) problems are independent; no collective on the data path);
+value = total flops of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused attn+A2A-layout TFLOP/s & % bf16 peak; fused vs serial time (1 GB300)"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_FILE = os.path.join(ROOT, "profiles", "ncu_attn_fused_image_dit.md")
+KERNEL_SOURCES = ("all_layout_gb300/csrc/attn.cu", "all_layout_gb300/csrc/ptx.cuh",
+                  "all_layout_gb300/csrc/internal.h")
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("xs", "reference"), default="xs")
+    ap.add_argument("--workload", default="image_dit")
+    ap.add_argument("--store-tile", type=int, default=None)
+    ap.add_argument("--side-steps", type=int, default=100,
+                    help="steps for the attention-alone / serial / scatter side timings")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    try:
+        text = open(PROFILE_FILE).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", text)
+    tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not tb or sha.group(1) != kernel_sha():
+        return None
+    return float(tb.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(w, rows_per_head: int, threads: int | None = None):
+    """Time the fp64 oracle on a row sample of workload w; returns (TFLOP/s, seconds,
+    threads, description)."""
+    import numpy as np
+    import oracle
+    from all_layout_gb300 import inputs
+    q, k, v = inputs.qkv(w.B, w.N, w.H, w.d, w.seed, w.q_scale)
+    rows = np.linspace(0, w.N - 1, rows_per_head).astype(np.int64)
+    thr = threads or oracle.default_threads()
+    oracle.attention_rows(q[:, :1, :8], k[:, :1, :8], v[:, :1, :8], rows[:1] % 8)  # load/build
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, rows, threads=thr)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.B * w.H * rows.size * w.N * w.d
+    desc = (f"{rows.size} query rows per head x {w.B * w.H} heads of {w.name} "
+            f"({flops:.3g} flops, {rows.size / w.N:.2%} of the workload)")
+    return flops / dt / 1e12, dt, thr, desc
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the fp64 CPU oracle on a bounded sample per step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from all_layout_gb300 import inputs
+    q, k, v = inputs.qkv(w.B, w.N, w.H, w.d, w.seed, w.q_scale)
+    thr = oracle.default_threads()
+    rows_per_step = 1
+    rows_all = np.arange(w.N, dtype=np.int64)
+    oracle.attention_rows(q, k, v, rows_all[:1], threads=thr)
+    for i in range(args.warmup):
+        oracle.attention_rows(q, k, v, rows_all[i % w.N: i % w.N + rows_per_step], threads=thr)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * 97) % (w.N - rows_per_step + 1)
+        oracle.attention_rows(q, k, v, rows_all[r0:r0 + rows_per_step], threads=thr)
+    dt = time.perf_counter() - t0
+    flops_step = 4.0 * w.B * w.H * rows_per_step * w.N * w.d
+    value = flops_step * args.steps / dt / 1e12
+    sample = (f"each step: {rows_per_step} query row per head x {w.B * w.H} heads of {w.name} "
+              f"({flops_step:.3g} flops, fp64, exact attention + layout definition)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "H": w.H, "d": w.d, "P": w.P},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_xs(args, w, rank, world, local):
+    import torch
+
+    from all_layout_gb300 import inputs, xs
+
+    st = args.store_tile or w.store_tile
+    dev = torch.device("cuda", local)
+    q_h, k_h, v_h = inputs.workload_qkv(w)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    shards = xs.alloc_shards(w.B, w.N, w.H, w.d, w.P, device=dev)
+    o = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused():
+        xs.attn_fused(q, k, v, shards, store_tile=st, stream=stream)
+
+    def timed(fn, steps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush.zero_()                 # L2 flush, outside the timed events
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev]   # ms
+
+    for _ in range(max(3, args.warmup)):
+        fused()
+    torch.cuda.synchronize(dev)
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    with ClockSampler(gpu_index) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        step_ms = timed(fused, args.steps)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        t1 = time.time()
+    if xs.last_device_status(stream) != xs.OK:
+        raise RuntimeError("an on-chip wait timed out during the timed region")
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    flops = w.flops
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    clocks = clk.summary(t0, t1)
+
+    # Side timings on the same GPU: attention alone, serial path, layout kernel alone.
+    side = max(5, args.side_steps)
+    t_attn = sorted(timed(lambda: xs.attn(q, k, v, o, stream=stream), side))
+    t_serial = sorted(timed(lambda: xs.attn_serial(q, k, v, o, shards, stream=stream), side))
+    t_scatter = sorted(timed(lambda: xs.scatter(o, shards, stream=stream), side))
+    med = lambda a: a[len(a) // 2]
+    t_fused_med = med(sorted(step_ms))
+
+    # End to end through the public API with host buffers: pinned H2D of q, k, v,
+    # the fused call, D2H of every shard, all inside the timed region.
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+        outs = [torch.empty(s.shape, dtype=s.dtype).pin_memory() for s in shards]
+        e2e_steps = max(5, min(args.steps, 200))
+
+        def e2e_step():
+            for hd, dd in ((qp, q), (kp, k), (vp, v)):
+                dd.copy_(hd, non_blocking=True)
+            xs.attn_fused(q, k, v, shards, store_tile=st, stream=stream)
+            for so, sd in zip(outs, shards):
+                so.copy_(sd, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e_ms = max_over_ranks(sum(timed(e2e_step, e2e_steps)), world) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+        d2h = sum(s.numel() * s.element_size() for s in shards)
+        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    pk, pk_kind = peaks()
+    peak = float(pk["bf16_tflops"])
+    achieved = flops / (ms_per_step * 1e-3) / 1e12        # per launch, this rank's GPU
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": f"{pk_kind} bf16 (burst)",
+                "traffic": profiled_traffic(), "kernel": "attn_kernel<%d> (fused)" % w.d,
+                "kernel_sha": kernel_sha()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = 256 if w.N <= 8192 else 32
+        val, dt, thr, desc = cpu_oracle_sample(w, rows)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "H": w.H, "d": w.d, "P": w.P,
+                       "store_tile": st, "seed": w.seed,
+                       "l2": "flushed between timed steps (512 MiB write, outside the events)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "t_fused_ms": t_fused_med, "t_attn_ms": med(t_attn), "t_serial_ms": med(t_serial),
+            "t_scatter_ms": med(t_scatter),
+            "fused_over_attn": t_fused_med / med(t_attn),
+            "serial_over_fused": med(t_serial) / t_fused_med,
+            "hiding_ratio": (med(t_serial) - t_fused_med) / med(t_scatter),
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    from all_layout_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, rank, world)
+        else:
+            run_xs(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

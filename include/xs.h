@@ -1,0 +1,125 @@
+/*
+ * xs.h - C ABI of libxs: non-causal attention fused with the post-attention
+ * Ulysses All-to-All layout, for one GB300 (sm_103a).
+ *
+ * Source of the operations: "X-Stage: An Overlooked Pipeline Stage for
+ * Communication-Computation Overlap in DiT Inference" (arXiv 2607.23264).
+ *  - Abstract: for Ulysses sequence-parallel attention, the post-attention
+ *    All-to-All is fused tile by tile into FlashAttention, so that the owner of
+ *    an output tile issues its stores itself and resumes computation, with no
+ *    dedicated communication warp or SM; compared against serial execution
+ *    (FlashAttention, then the All-to-All) and FlashAttention alone.
+ *  - Figure 5 (d)-(e): FlashAttention produces each head partition's output and
+ *    the post-attention All-to-All restores the original sequence partition.
+ *  - Figure 1 / Figure 7: the stores of one output tile drain while the next
+ *    mainloop computes (the piggybacked FlashAttention-A2A pipeline).
+ *
+ * What every attention entry point computes, per batch b and head h:
+ *     o[b][h][n][:] = softmax_j( q[b][h][n][:] . k[b][h][j][:] / sqrt(d) ) v[b][h][j][:]
+ * over all N keys (non-causal, no mask, no dropout), fp32 accumulation, output
+ * rounded to bf16 (round to nearest even).
+ *
+ * The layout ("shards"): destination p (0 <= p < P) receives the contiguous
+ * sequence block [p*N/P, (p+1)*N/P) of every head:
+ *     shard_p[b][i][h][c] = o[b][h][p*(N/P) + i][c],   0 <= i < N/P.
+ * On one GPU the P destinations are P separate device buffers.
+ *
+ * Conventions shared by all calls
+ *  - Element type: every buffer is bf16 (2 bytes), in device memory.
+ *  - q, k, v, o: [B][H][N][d], contiguous (d fastest).
+ *  - shard p: [B][N/P][H][d], contiguous; out_shards is a HOST array of P
+ *    device pointers, read during the call (the array may be freed afterwards).
+ *  - Ownership: the caller owns every buffer. The library allocates no device
+ *    memory; it keeps only a device status word (see xs_last_device_status).
+ *  - Asynchrony: each call only enqueues work on `stream` (a cudaStream_t; NULL
+ *    means the legacy default stream) and returns without synchronising. Launch
+ *    errors are reported as XS_ERR_CUDA. Kernel-side waits are bounded: a wait
+ *    that runs out records XS_ERR_TIMEOUT in the status word and the kernel
+ *    returns, leaving the context usable.
+ *  - Aliasing: inputs, outputs and shards must not overlap.
+ *  - Threads: calls on different streams are independent.
+ *  - Validation, in this order, before any device work:
+ *      XS_ERR_INVALID     a NULL pointer (also any NULL shard), B, N or H < 0,
+ *                         P not in [1, 8], N % P != 0,
+ *                         store_tile not in {1, 2, 4, 8};
+ *      XS_ERR_UNSUPPORTED d not in {64, 128}, or N % 128 != 0;
+ *      XS_ERR_ALIGN       a pointer that is not 16-byte aligned.
+ *    B == 0, H == 0 or N == 0 is an empty problem: the call validates its
+ *    other arguments and returns XS_OK without launching anything.
+ */
+#ifndef XS_H
+#define XS_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  XS_OK = 0,
+  XS_ERR_INVALID = 1,
+  XS_ERR_UNSUPPORTED = 2,
+  XS_ERR_ALIGN = 3,
+  XS_ERR_CUDA = 4,
+  XS_ERR_TIMEOUT = 5
+} xs_status;
+
+/* Fused attention + shard layout (abstract: tile-granular fusion of the
+ * post-attention All-to-All with FlashAttention; Figure 7). One persistent
+ * kernel. Each finished 128-row output tile is staged on chip and written into
+ * the P shards by the warps that own it, in bursts of `store_tile` 16-row slabs
+ * interleaved with the KV iterations of that warp group's next tile
+ * (store_tile = 8: the whole tile right after it is finished).
+ * The result does not depend on store_tile.
+ *   q, k, v     [B][H][N][d] bf16, device.
+ *   out_shards  host array of P device pointers, shard p [B][N/P][H][d] bf16.
+ *   store_tile  1, 2, 4 or 8 slabs per burst. */
+xs_status xs_attn_fused(const void *q, const void *k, const void *v,
+                        void *const *out_shards, int B, int N, int H, int d,
+                        int P, int store_tile, void *stream);
+
+/* Attention alone (the FlashAttention-alone time the abstract compares the
+ * fused kernel with): same kernel, output written head-major to
+ * o [B][H][N][d] bf16 (device). */
+xs_status xs_attn(const void *q, const void *k, const void *v, void *o, int B,
+                  int N, int H, int d, void *stream);
+
+/* The layout alone (the separate post-attention All-to-All of serial
+ * execution, Figure 5 (e)), as a bit-exact copy kernel:
+ * o [B][H][N][d] -> shards. Any 16-bit payload is copied unchanged. */
+xs_status xs_scatter(const void *o, void *const *out_shards, int B, int N,
+                     int H, int d, int P, void *stream);
+
+/* Serial execution (abstract: the baseline of the sender-visible speedup):
+ * xs_attn into the caller's o_scratch [B][H][N][d] bf16, then xs_scatter into
+ * the shards, two launches on `stream`. o_scratch holds o afterwards. */
+xs_status xs_attn_serial(const void *q, const void *k, const void *v,
+                         void *o_scratch, void *const *out_shards, int B, int N,
+                         int H, int d, int P, void *stream);
+
+/* Static English text for a status code; never NULL. */
+const char *xs_status_string(xs_status s);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word for the current device: XS_ERR_TIMEOUT if a kernel's bounded wait ran
+ * out since the last call, XS_ERR_CUDA if the synchronisation failed, else
+ * XS_OK. For tests and debugging; the attention calls never block on it. */
+xs_status xs_last_device_status(void *stream);
+
+/* Sets the limit, in nanoseconds, after which a kernel's on-chip wait gives up
+ * (default 2e9 = 2 s; 0 restores the default). Applies to later launches from
+ * this process. Returns the previous limit. */
+unsigned long long xs_set_wait_limit_ns(unsigned long long limit_ns);
+
+/* Self-test of the bounded wait: launches one CTA that waits on an on-chip
+ * barrier that nothing ever signals, with the current wait limit. The wait
+ * must run out, record XS_ERR_TIMEOUT in the status word and return. Read the
+ * outcome with xs_last_device_status. */
+xs_status xs_selftest_bounded_wait(void *stream);
+
+/* ABI version of this header (1). */
+int xs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XS_H */

@@ -1,0 +1,192 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Floating-point outputs must satisfy |err| <= 1e-2 + 1e-2*|ref| elementwise and a
+relative RMS <= 1e-2; placement and the layout kernel must be bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from all_layout_gb300 import inputs
+from gpu_util import assert_close, gather_rows, sample_rows, shards_bits, shards_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def xs():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    from all_layout_gb300 import xs as _xs
+    torch.cuda.set_device(0)
+    return _xs
+
+
+def _dev(*ts):
+    return tuple(t.cuda() for t in ts)
+
+
+def _run_fused(xs, q, k, v, P, st=8):
+    B, H, N, d = q.shape
+    shards = xs.alloc_shards(B, N, H, d, P)
+    for s in shards:
+        s.fill_(float("nan"))
+    xs.attn_fused(*_dev(q, k, v), shards, store_tile=st)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    return shards
+
+
+# ------------------------------------------------------------------ layout kernel
+
+@pytest.mark.parametrize("B,H,N,d,P", [(1, 4, 256, 64, 2), (2, 3, 384, 128, 3), (1, 24, 1024, 128, 8),
+                                       (2, 5, 640, 64, 5), (1, 2, 128, 128, 1), (1, 7, 896, 64, 7)])
+def test_scatter_bit_exact(xs, B, H, N, d, P):
+    o = inputs.tags(B, N, H, d, seed=N + P)
+    shards = xs.alloc_shards(B, N, H, d, P)
+    xs.scatter(o.cuda(), shards)
+    torch.cuda.synchronize()
+    exp = oracle.shard_layout(inputs.bits(o), P)
+    assert np.array_equal(shards_bits(shards), exp)
+
+
+# ------------------------------------------------------------------ bounded waits
+
+def test_bounded_wait_times_out_and_context_survives(xs):
+    assert xs.last_device_status() == xs.OK
+    old = xs.set_wait_limit_ns(2_000_000)        # 2 ms
+    try:
+        xs.selftest_bounded_wait()
+        assert xs.last_device_status() == xs.ERR_TIMEOUT
+        assert xs.last_device_status() == xs.OK    # the status word was cleared
+    finally:
+        xs.set_wait_limit_ns(old)
+    # the context is still usable
+    q, k, v = inputs.qkv(1, 256, 2, 64, seed=11)
+    shards = _run_fused(xs, q, k, v, 2)
+    assert_close(shards_f64(shards), oracle.shard_layout(oracle.attention(q, k, v), 2))
+
+
+# ------------------------------------------------------------------ small workload
+
+def test_small_fused_all_store_tiles(xs):
+    w = inputs.WORKLOADS["small"]
+    q, k, v = inputs.workload_qkv(w)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), w.P)
+    outs = []
+    for st in (1, 2, 4, 8):
+        shards = _run_fused(xs, q, k, v, w.P, st)
+        assert_close(shards_f64(shards), ref, f"store_tile={st}")
+        outs.append(shards_bits(shards))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "output depends on store_tile"
+
+
+def test_small_attention_alone_and_serial(xs):
+    w = inputs.WORKLOADS["small"]
+    q, k, v = inputs.workload_qkv(w)
+    o_ref = oracle.attention(q, k, v)
+    qd, kd, vd = _dev(q, k, v)
+    o = torch.empty_like(qd)
+    xs.attn(qd, kd, vd, o)
+    torch.cuda.synchronize()
+    assert_close(o.float().cpu().numpy(), o_ref, "attention alone")
+    shards = xs.alloc_shards(w.B, w.N, w.H, w.d, w.P)
+    scratch = torch.empty_like(qd)
+    xs.attn_serial(qd, kd, vd, scratch, shards)
+    torch.cuda.synchronize()
+    assert_close(shards_f64(shards), oracle.shard_layout(o_ref, w.P), "serial")
+    fused = _run_fused(xs, q, k, v, w.P)
+    # same arithmetic, different destinations: fused and serial agree bit for bit
+    assert np.array_equal(shards_bits(shards), shards_bits(fused))
+    assert np.array_equal(scratch.cpu().view(torch.int16).numpy(), o.cpu().view(torch.int16).numpy())
+
+
+# ------------------------------------------------------------------ exact placement
+
+@pytest.mark.parametrize("B,H,N,d,P", [(2, 2, 1024, 128, 4), (1, 3, 512, 64, 8), (1, 2, 384, 128, 3),
+                                       (1, 1, 128, 64, 1)])
+@pytest.mark.parametrize("st", [1, 8])
+def test_one_hot_exact_placement(xs, B, H, N, d, P, st):
+    q, k, v, perm = inputs.one_hot_case(B, N, H, d, seed=17)
+    shards = _run_fused(xs, q, k, v, P, st)
+    vb = inputs.bits(v)
+    o_exp = np.take_along_axis(vb, perm[..., None].repeat(d, axis=3), axis=2)
+    exp = oracle.shard_layout(o_exp, P)
+    got = shards_bits(shards)
+    if not np.array_equal(got, exp):
+        bad = np.argwhere(got != exp)
+        raise AssertionError(f"{len(bad)} mismatching elements, first at {tuple(bad[0])}")
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+def test_zero_query_gives_column_mean(xs):
+    B, H, N, d, P = 1, 3, 512, 128, 4
+    _, k, v = inputs.qkv(B, N, H, d, seed=21)
+    v = (v.float() + 1.0).to(torch.bfloat16)
+    q = torch.zeros_like(k)
+    shards = _run_fused(xs, q, k, v, P)
+    mean = oracle.bf16_bits_to_f64(inputs.bits(v)).mean(axis=2, keepdims=True)
+    exp = oracle.shard_layout(np.broadcast_to(mean, (B, H, N, d)).copy(), P)
+    assert_close(shards_f64(shards), exp, "q=0")
+
+
+def test_identical_v_rows(xs):
+    B, H, N, d, P = 1, 2, 768, 64, 2
+    q, k, _ = inputs.qkv(B, N, H, d, seed=22, q_scale=4.0)
+    row = inputs.qkv(B, 1, H, d, seed=23)[2]
+    v = row.expand(B, H, N, d).contiguous()
+    shards = _run_fused(xs, q, k, v, P)
+    exp = oracle.shard_layout(np.broadcast_to(oracle.bf16_bits_to_f64(inputs.bits(row)),
+                                              (B, H, N, d)).copy(), P)
+    assert_close(shards_f64(shards), exp, "identical V rows")
+
+
+# ------------------------------------------------------------------ shapes and ragged work
+
+@pytest.mark.parametrize("B,H,N,d,P,qs", [
+    (1, 2, 384, 128, 3, 1.0),     # odd tile count: the last unit has one tile
+    (2, 3, 512, 64, 4, 1.0),      # several batches
+    (1, 3, 640, 128, 5, 4.0),     # 5 tiles, peaked rows
+    (1, 1, 128, 128, 1, 1.0),     # one tile, one KV step
+    (3, 1, 256, 64, 8, 2.0),      # 32-row shards: a tile spans 4 shards
+])
+def test_shapes_vs_oracle(xs, B, H, N, d, P, qs):
+    q, k, v = inputs.qkv(B, N, H, d, seed=31 + N + P, q_scale=qs)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    for st in (2, 8):
+        assert_close(shards_f64(_run_fused(xs, q, k, v, P, st)), ref, f"st={st}")
+
+
+def test_image_dit_full(xs):
+    w = inputs.WORKLOADS["image_dit"]
+    q, k, v = inputs.workload_qkv(w)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), w.P)
+    assert_close(shards_f64(_run_fused(xs, q, k, v, w.P, w.store_tile)), ref, w.name)
+
+
+@pytest.mark.parametrize("key", ["peaked_16k", "video_dit"])
+def test_long_sequences_sampled(xs, key):
+    w = inputs.WORKLOADS[key]
+    q, k, v = inputs.workload_qkv(w)
+    shards = _run_fused(xs, q, k, v, w.P, w.store_tile)
+    got = shards_f64(shards)
+    rng = np.random.default_rng(w.seed)
+    rows = sample_rows(w.N, w.P, rng, extra=8)
+    ref = oracle.attention_rows(q, k, v, rows)
+    assert_close(gather_rows(got, rows, w.N, w.P), ref, w.name)
+    # every shard fully written (no NaN left from the fill)
+    assert np.all(np.isfinite(got))
+
+
+@pytest.mark.parametrize("idx", [5, 30, 55, 89])
+def test_sweep_points_sampled(xs, idx):
+    w = inputs.sweep_points()[idx]
+    q, k, v = inputs.workload_qkv(w)
+    got = shards_f64(_run_fused(xs, q, k, v, w.P, w.store_tile))
+    rows = sample_rows(w.N, w.P, np.random.default_rng(w.seed), extra=8)
+    assert_close(gather_rows(got, rows, w.N, w.P), oracle.attention_rows(q, k, v, rows), w.name)
+    assert np.all(np.isfinite(got))
