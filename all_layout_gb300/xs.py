@@ -37,7 +37,8 @@ _lib.xs_attn_fused.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _i, _vp]
 _lib.xs_attn.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.xs_scatter.argtypes = [_vp, _PP, _i, _i, _i, _i, _i, _vp]
 _lib.xs_attn_serial.argtypes = [_vp, _vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
-for _f in ("xs_attn_fused", "xs_attn", "xs_scatter", "xs_attn_serial",
+_lib.xs_attn_serial_noalloc.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
+for _f in ("xs_attn_fused", "xs_attn", "xs_scatter", "xs_attn_serial", "xs_attn_serial_noalloc",
            "xs_last_device_status", "xs_selftest_bounded_wait"):
     getattr(_lib, _f).restype = _i
 _lib.xs_status_string.argtypes = [_i]
@@ -130,6 +131,15 @@ def attn_serial(q, k, v, o_scratch, shards, stream=None):
     pp, keep = _shard_array(shards)
     _check(_lib.xs_attn_serial(_ptr(q), _ptr(k), _ptr(v), _ptr(o_scratch), pp, B, N, H, d,
                                len(shards), _stream(stream)), "xs_attn_serial")
+
+
+def attn_serial_noalloc(q, k, v, shards, stream=None):
+    """Serial execution with the intermediate o kept in the library's fixed
+    scratch array (no device allocation; see xs_attn_serial_noalloc in xs.h)."""
+    B, N, H, d = _dims(q)
+    pp, keep = _shard_array(shards)
+    _check(_lib.xs_attn_serial_noalloc(_ptr(q), _ptr(k), _ptr(v), pp, B, N, H, d, len(shards),
+                                       _stream(stream)), "xs_attn_serial_noalloc")
 
 
 def last_device_status(stream=None) -> int:

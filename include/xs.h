@@ -30,7 +30,8 @@
  *  - shard p: [B][N/P][H][d], contiguous; out_shards is a HOST array of P
  *    device pointers, read during the call (the array may be freed afterwards).
  *  - Ownership: the caller owns every buffer. The library allocates no device
- *    memory; it keeps only a device status word (see xs_last_device_status).
+ *    memory; it keeps only a device status word (see xs_last_device_status)
+ *    and the fixed scratch array of xs_attn_serial_noalloc.
  *  - Asynchrony: each call only enqueues work on `stream` (a cudaStream_t; NULL
  *    means the legacy default stream) and returns without synchronising. Launch
  *    errors are reported as XS_ERR_CUDA. Kernel-side waits are bounded: a wait
@@ -95,6 +96,33 @@ xs_status xs_scatter(const void *o, void *const *out_shards, int B, int N,
 xs_status xs_attn_serial(const void *q, const void *k, const void *v,
                          void *o_scratch, void *const *out_shards, int B, int N,
                          int H, int d, int P, void *stream);
+
+/* Size of the scratch array that xs_attn_serial_noalloc uses: 32 MiB. */
+#define XS_NOALLOC_SCRATCH_BYTES (32ull << 20)
+
+/* Serial execution without a caller-supplied intermediate buffer, for callers
+ * that cannot allocate device memory (for example code embedded in a host
+ * framework that owns all device memory through its own allocator or a fixed
+ * memory plan, or loops where a cudaMalloc would synchronise the device).
+ * The paper has no counterpart to this entry point; it only changes where the
+ * intermediate o of xs_attn_serial lives.
+ * Same arguments, results and validation as xs_attn_serial minus o_scratch:
+ * the intermediate o [B][H][N][d] bf16 lives in one array of
+ * XS_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library holds until the process exits. Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library call.
+ *   - XS_ERR_INVALID if B*H*N*d*2 bytes exceed XS_NOALLOC_SCRATCH_BYTES
+ *     (checked first, before any device work).
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves the last call's o
+ *     in it (each call overwrites all of the o it reads, so nothing needs
+ *     clearing). Calls that overlap on the GPU (different streams, or
+ *     different host threads without ordering) race on the array. */
+xs_status xs_attn_serial_noalloc(const void *q, const void *k, const void *v,
+                                 void *const *out_shards, int B, int N, int H,
+                                 int d, int P, void *stream);
 
 /* Static English text for a status code; never NULL. */
 const char *xs_status_string(xs_status s);
