@@ -52,6 +52,7 @@ constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kHalfBytes = BM * 128;     // one 64-column half of a 128-row tile
+constexpr int kPrefetchAhead = 4;          // K/V tiles warmed in L2 ahead of their loads
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 template <int D>
@@ -84,11 +85,10 @@ __device__ __forceinline__ void record_timeout(volatile int *abort_flag) {
   atomicExch(&g_status, kDevTimeout);
 }
 
-// Bounded wait on a barrier phase. Gives up when another role has aborted or
-// when `limit` ns pass, in which case it records a timeout.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                        uint64_t limit) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait on a barrier phase, slow path. Gives up when another role has
+// aborted or when `limit` ns pass, in which case it records a timeout.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity,
+                                             volatile int *abort_flag, uint64_t limit) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -100,6 +100,12 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, abort_flag, limit);
 }
 
 // Wait used while tearing down after an abort: ignores the abort flag, still bounded.
@@ -136,7 +142,28 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
       tma_load_3d(smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), &p.tm_q, q_full, hf * 64,
                   q0b, bh);
     }
+    {
+      // Warm L2 with the next unit's query tiles and this unit's first K/V tiles.
+      const int un = u + gridDim.x;
+      if (un < p.n_units) {
+        const int bhn = un / p.n_pairs, pn = un % p.n_pairs;
+        for (int hf = 0; hf < C::NH; ++hf) {
+          tma_prefetch_l2_3d(&p.tm_q, hf * 64, pn * 2 * BM, bhn);
+          if (2 * pn + 1 < p.n_qtiles) tma_prefetch_l2_3d(&p.tm_q, hf * 64, pn * 2 * BM + BM, bhn);
+        }
+      }
+      for (int j = 0; j < kPrefetchAhead && j < p.n_kv; ++j)
+        for (int hf = 0; hf < C::NH; ++hf) {
+          tma_prefetch_l2_3d(&p.tm_k, hf * 64, j * BN, bh);
+          tma_prefetch_l2_3d(&p.tm_v, hf * 64, j * BN, bh);
+        }
+    }
     for (int j = 0; j < p.n_kv; ++j) {
+      if (j + kPrefetchAhead < p.n_kv)
+        for (int hf = 0; hf < C::NH; ++hf) {
+          tma_prefetch_l2_3d(&p.tm_k, hf * 64, (j + kPrefetchAhead) * BN, bh);
+          tma_prefetch_l2_3d(&p.tm_v, hf * 64, (j + kPrefetchAhead) * BN, bh);
+        }
       for (int kind = 0; kind < 2; ++kind, ++it) {
         const uint32_t slot = it % C::KV_STAGES, ph = (it / C::KV_STAGES) & 1;
         if (!wait_phase(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) goto drain;
@@ -160,34 +187,30 @@ drain:
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// Descriptors are built once per tile buffer; the k-th MMA of a tile only adds a
+// constant to the start-address field (the low 14 bits hold address >> 4 and
+// shared addresses stay below 256 KiB, so the add never carries out of it).
+// This keeps the single issuing thread's work per MMA to a couple of
+// instructions, so issue never trails the tensor pipe.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint8_t *smem, uint32_t tmem, int t, uint32_t slot) {
-  using C = Cfg<D>;
+__device__ __forceinline__ void issue_qk(uint32_t dcol, uint64_t qdesc, uint64_t kdesc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0);
-  const uint32_t qb = smem_u32(smem + C::OFF_Q + t * C::TILE);
-  const uint32_t kb = smem_u32(smem + C::OFF_KV + slot * C::TILE);
-  const uint32_t dcol = tmem + (t == 0 ? C::COL_S0 : C::COL_S1);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * kHalfBytes + (kk % 4) * 32;
-    tc_mma_ss(dcol, smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idesc,
-              kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(((kk / 4) * kHalfBytes + (kk % 4) * 32) >> 4);
+    tc_mma_ss(dcol, qdesc + off, kdesc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint8_t *smem, uint32_t tmem, int t, uint32_t slot,
+__device__ __forceinline__ void issue_pv(uint32_t dcol, uint32_t pcol, uint64_t vdesc,
                                          uint32_t accumulate) {
-  using C = Cfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, 1);
-  const uint32_t vb = smem_u32(smem + C::OFF_KV + slot * C::TILE);
-  const uint32_t pcol = tmem + (t == 0 ? C::COL_S0 : C::COL_S1);
-  const uint32_t dcol = tmem + (t == 0 ? C::COL_O0 : C::COL_O1);
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
     // V is the MN-major B operand: 16 key rows per MMA (2 KiB of the swizzled
-    // tile), the next 64 columns of d one half (kHalfBytes) further.
-    tc_mma_ts(dcol, pcol + kk * 8, smem_desc_sw128(vb + kk * 2048, kHalfBytes, 1024), idesc,
+    // tile); the next 64 columns of d sit one half (kHalfBytes, the LBO) further.
+    tc_mma_ts(dcol, pcol + kk * 8, vdesc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
               (kk > 0 || accumulate) ? 1u : 0u);
   }
 }
@@ -202,6 +225,17 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
   const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
   auto kv_full = [&](uint32_t s) { return smem_u32(&bars->kv_full[s]); };
   auto kv_empty = [&](uint32_t s) { return smem_u32(&bars->kv_empty[s]); };
+  uint64_t qdesc[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    qdesc[t] = smem_desc_sw128(smem_u32(smem + C::OFF_Q + t * C::TILE), 16, 1024);
+  // Slot s of the K/V ring starts s * TILE bytes after slot 0: add (s * TILE) >> 4.
+  const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
+  const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + C::OFF_KV), kHalfBytes, 1024);
+  auto kdesc = [&](uint32_t s) { return kdesc0 + static_cast<uint64_t>(s * (C::TILE >> 4)); };
+  auto vdesc = [&](uint32_t s) { return vdesc0 + static_cast<uint64_t>(s * (C::TILE >> 4)); };
+  const uint32_t col_s[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
+  const uint32_t col_o[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
     if (!wait_phase(q_full, lu & 1, abort_flag, lim)) goto drain;
     {
@@ -209,7 +243,7 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
       if (!wait_phase(kv_full(sk), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
       tc_fence_after();
       for (int t = 0; t < 2; ++t) {
-        issue_qk<D>(smem, tmem, t, sk);
+        issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
         tc_commit(smem_u32(&bars->s_full[t]));
       }
       tc_commit(kv_empty(sk));
@@ -219,16 +253,18 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
     for (int j = 1; j < p.n_kv; ++j) {
       const uint32_t sv = it % C::KV_STAGES, sk = (it + 1) % C::KV_STAGES;
       if (!wait_phase(kv_full(sv), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
-      if (!wait_phase(kv_full(sk), ((it + 1) / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
       for (int t = 0; t < 2; ++t) {
         if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
         ++pc[t];
         tc_fence_after();
-        issue_pv<D>(smem, tmem, t, sv, j > 1 ? 1u : 0u);
-        issue_qk<D>(smem, tmem, t, sk);
+        issue_pv<D>(col_o[t], col_s[t], vdesc(sv), j > 1 ? 1u : 0u);
+        if (t == 1) tc_commit(kv_empty(sv));   // V(j-1) is free once PV1 is done
+        // K(j) is needed only now: PV0 above never waits for it.
+        if (t == 0 && !wait_phase(kv_full(sk), ((it + 1) / C::KV_STAGES) & 1, abort_flag, lim))
+          goto drain;
+        issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
         tc_commit(smem_u32(&bars->s_full[t]));
       }
-      tc_commit(kv_empty(sv));
       tc_commit(kv_empty(sk));
       it += 2;
       if (j == p.n_kv - 1) tc_commit(q_empty);
@@ -240,7 +276,7 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
         if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
         ++pc[t];
         tc_fence_after();
-        issue_pv<D>(smem, tmem, t, sv, p.n_kv > 1 ? 1u : 0u);
+        issue_pv<D>(col_o[t], col_s[t], vdesc(sv), p.n_kv > 1 ? 1u : 0u);
         tc_commit(smem_u32(&bars->o_full[t]));
       }
       tc_commit(kv_empty(sv));
@@ -324,11 +360,25 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
       tmem_wait_ld();
-      float mx = __uint_as_float(s[0][0]);
+      // Row max as 8 independent chains, then a tree (short dependency chain).
+      float mp[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int i = 0; i < 8; ++i)
+        mp[i] = fmaxf(__uint_as_float(s[0][i]), __uint_as_float(s[0][i + 8]));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
+      for (int i = 0; i < 8; ++i)
+        mp[i] = fmaxf(mp[i], fmaxf(__uint_as_float(s[0][i + 16]), __uint_as_float(s[0][i + 24])));
+#pragma unroll
+      for (int c = 1; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mp[i] = fmaxf(mp[i], __uint_as_float(s[c][8 * k + i]));
+#pragma unroll
+      for (int w = 4; w >= 1; w /= 2)
+#pragma unroll
+        for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
+      const float mx = mp[0];
       const float m_new = fmaxf(m, mx * scale);
       // Conditional rescale: keep the running max unless it grew by more than
       // 2^kRescaleThreshold, so O is rescaled only on the rare large jumps.
@@ -346,8 +396,8 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
           }
         }
       }
-      l *= alpha;
       const float neg_m = -m;
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};   // row sum as 4 independent chains
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -355,11 +405,12 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i]), scale, neg_m));
           const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i + 1]), scale, neg_m));
-          l += p0 + p1;
+          lp[i % 4] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the S columns already read
       }
+      l = fmaf(l, alpha, (lp[0] + lp[1]) + (lp[2] + lp[3]));
       if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
