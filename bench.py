@@ -328,7 +328,7 @@ def run_xs(args, w, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows = 256 if w.N <= 8192 else 32
+        rows = w.N if w.N <= 8192 else 256     # whole workload when it takes seconds
         val, dt, thr, desc = cpu_oracle_sample(w, rows)
         cpu = {"value": val, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
                "seconds": dt}
