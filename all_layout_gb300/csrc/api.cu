@@ -136,6 +136,8 @@ xs_status launch_attention(const void *q, const void *k, const void *v, void *o,
   prm.N = N;
   prm.H = H;
   prm.store_tile = store_tile;
+  prm.shared_staging = store_tile == 8 ? 1 : 0;
+  prm.kv_stages = xs::attn_kv_stages(d, store_tile == 8);
   prm.n_qtiles = N / xs::kTileRows;
   prm.n_pairs = (prm.n_qtiles + 1) / 2;
   prm.n_units = B * H * prm.n_pairs;

@@ -52,33 +52,40 @@ constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kHalfBytes = BM * 128;     // one 64-column half of a 128-row tile
+constexpr uint32_t kWaitSleepNs = 100000;   // longest suspension per try in a blocked wait
 constexpr int kPrefetchAhead = 4;          // K/V tiles warmed in L2 ahead of their loads
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
-template <int D>
+template <int D, bool SHARED>
 struct Cfg {
   static constexpr int NH = D / 64;
   static constexpr int TILE = BM * D * 2;
-  static constexpr int KV_STAGES = (D == 128) ? 3 : 6;
+  // After the two Q tiles come NREG tile-sized regions shared by the K/V ring and
+  // the output staging: with store_tile = 8 the two warp groups take turns on one
+  // staging tile (NREG-1 ring slots); with deferred bursts each group keeps its
+  // own staging tile (NREG-2 ring slots).
+  static constexpr int NREG = (D == 128) ? 5 : 11;
+  static constexpr int MAX_STAGES = NREG - 1;
+  static constexpr int KV_STAGES = SHARED ? NREG - 1 : NREG - 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * TILE;
-  static constexpr int OFF_STG = OFF_KV + KV_STAGES * TILE;
-  static constexpr int OFF_BAR = OFF_STG + 2 * TILE;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
+  static constexpr int OFF_BAR = OFF_KV + NREG * TILE;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;   // + slack to align the base to 1024
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
   static constexpr uint32_t COL_O0 = 256, COL_O1 = 256 + D;
 };
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[6], kv_empty[6];
+  uint64_t kv_full[10], kv_empty[10];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t wg_sync[2];
   uint64_t drain;
+  uint64_t stg_free;   // shared staging tile released (one arrival per use)
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block too large");
+static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
 __device__ __forceinline__ void record_timeout(volatile int *abort_flag) {
   *abort_flag = 1;
@@ -91,7 +98,7 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity,
                                              volatile int *abort_flag, uint64_t limit) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if ((it & 15u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > limit) {
@@ -122,10 +129,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 // ------------------------------------------------------------------ TMA loader
-template <int D>
+template <int D, bool SHARED>
 __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volatile int *abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, SHARED>;
   const uint64_t lim = p.wait_limit_ns;
+  constexpr uint32_t stages = C::KV_STAGES;
   uint32_t it = 0;          // K/V slot uses so far (K and V each take one)
   uint32_t q_armed = 0;     // q_full phases armed so far
   uint32_t lu = 0;          // units processed by this CTA
@@ -165,7 +173,7 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
           tma_prefetch_l2_3d(&p.tm_v, hf * 64, (j + kPrefetchAhead) * BN, bh);
         }
       for (int kind = 0; kind < 2; ++kind, ++it) {
-        const uint32_t slot = it % C::KV_STAGES, ph = (it / C::KV_STAGES) & 1;
+        const uint32_t slot = it % stages, ph = (it / stages) & 1;
         if (!wait_phase(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) goto drain;
         const uint32_t full = smem_u32(&bars->kv_full[slot]);
         mbar_arrive_expect_tx(full, C::TILE);
@@ -179,9 +187,9 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
 drain:
   // Every load this thread issued must land before the CTA releases its smem:
   // wait for the most recently armed phase of each barrier it armed.
-  for (uint32_t s = 0; s < (uint32_t)C::KV_STAGES && s < it; ++s) {
-    const uint32_t last = s + ((it - 1 - s) / C::KV_STAGES) * C::KV_STAGES;  // last use of slot s
-    drain_phase(smem_u32(&bars->kv_full[s]), (last / C::KV_STAGES) & 1, lim);
+  for (uint32_t s = 0; s < stages && s < it; ++s) {
+    const uint32_t last = s + ((it - 1 - s) / stages) * stages;  // last use of slot s
+    drain_phase(smem_u32(&bars->kv_full[s]), (last / stages) & 1, lim);
   }
   if (q_armed > 0) drain_phase(q_full, (q_armed - 1) & 1, lim);
 }
@@ -215,11 +223,12 @@ __device__ __forceinline__ void issue_pv(uint32_t dcol, uint32_t pcol, uint64_t 
   }
 }
 
-template <int D>
+template <int D, bool SHARED>
 __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem,
                          volatile int *abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, SHARED>;
   const uint64_t lim = p.wait_limit_ns;
+  constexpr uint32_t stages = C::KV_STAGES;
   uint32_t it = 0, lu = 0;
   uint32_t pc[2] = {0, 0};
   const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
@@ -239,8 +248,8 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
     if (!wait_phase(q_full, lu & 1, abort_flag, lim)) goto drain;
     {
-      const uint32_t sk = it % C::KV_STAGES;
-      if (!wait_phase(kv_full(sk), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
+      const uint32_t sk = it % stages;
+      if (!wait_phase(kv_full(sk), (it / stages) & 1, abort_flag, lim)) goto drain;
       tc_fence_after();
       for (int t = 0; t < 2; ++t) {
         issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
@@ -251,8 +260,8 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
       if (p.n_kv == 1) tc_commit(q_empty);
     }
     for (int j = 1; j < p.n_kv; ++j) {
-      const uint32_t sv = it % C::KV_STAGES, sk = (it + 1) % C::KV_STAGES;
-      if (!wait_phase(kv_full(sv), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
+      const uint32_t sv = it % stages, sk = (it + 1) % stages;
+      if (!wait_phase(kv_full(sv), (it / stages) & 1, abort_flag, lim)) goto drain;
       for (int t = 0; t < 2; ++t) {
         if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
         ++pc[t];
@@ -260,7 +269,7 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
         issue_pv<D>(col_o[t], col_s[t], vdesc(sv), j > 1 ? 1u : 0u);
         if (t == 1) tc_commit(kv_empty(sv));   // V(j-1) is free once PV1 is done
         // K(j) is needed only now: PV0 above never waits for it.
-        if (t == 0 && !wait_phase(kv_full(sk), ((it + 1) / C::KV_STAGES) & 1, abort_flag, lim))
+        if (t == 0 && !wait_phase(kv_full(sk), ((it + 1) / stages) & 1, abort_flag, lim))
           goto drain;
         issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
         tc_commit(smem_u32(&bars->s_full[t]));
@@ -270,8 +279,8 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
       if (j == p.n_kv - 1) tc_commit(q_empty);
     }
     {
-      const uint32_t sv = it % C::KV_STAGES;
-      if (!wait_phase(kv_full(sv), (it / C::KV_STAGES) & 1, abort_flag, lim)) goto drain;
+      const uint32_t sv = it % stages;
+      if (!wait_phase(kv_full(sv), (it / stages) & 1, abort_flag, lim)) goto drain;
       for (int t = 0; t < 2; ++t) {
         if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
         ++pc[t];
@@ -298,7 +307,7 @@ struct StoreState {
 template <int D>
 __device__ __forceinline__ void issue_slabs(const AttnParams &p, const uint8_t *stg,
                                             StoreState<D> &ss, int count) {
-  using C = Cfg<D>;
+  using C = Cfg<D, false>;
   int issued = 0;
   while (ss.next < NSLAB && issued < count) {
     const int s = ss.next;
@@ -326,10 +335,30 @@ __device__ __forceinline__ void issue_slabs(const AttnParams &p, const uint8_t *
   if (issued) bulk_commit();
 }
 
-template <int D>
+// Running maxima over 64 raw scores (two 32-register chunks) in 8 independent
+// chains of 3-input max; `first` starts the chains.
+__device__ __forceinline__ void row_max_part(const uint32_t (&a)[32], const uint32_t (&b)[32],
+                                             float (&mp)[8], bool first) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x = __uint_as_float(a[i]), y = __uint_as_float(a[i + 8]);
+    mp[i] = first ? fmaxf(x, y) : max3(mp[i], x, y);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    mp[i] = max3(mp[i], __uint_as_float(a[i + 16]), __uint_as_float(a[i + 24]));
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    mp[i] = max3(mp[i], __uint_as_float(b[i]), __uint_as_float(b[i + 8]));
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    mp[i] = max3(mp[i], __uint_as_float(b[i + 16]), __uint_as_float(b[i + 24]));
+}
+
+template <int D, bool SHARED>
 __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem,
                              volatile int *abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, SHARED>;
   const uint64_t lim = p.wait_limit_ns;
   const int t = threadIdx.x / 128;          // warp group = query tile of the unit
   const int wq = (threadIdx.x / 32) & 3;    // warp within the group = TMEM lane quarter
@@ -341,7 +370,9 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
   const uint32_t tO = tmem + lane_base + (t == 0 ? C::COL_O0 : C::COL_O1);
   const uint32_t s_full = smem_u32(&bars->s_full[t]), p_full = smem_u32(&bars->p_full[t]);
   const uint32_t o_full = smem_u32(&bars->o_full[t]), wg_sync = smem_u32(&bars->wg_sync[t]);
-  uint8_t *stg = smem + C::OFF_STG + t * C::TILE;
+  constexpr bool shared_stg = SHARED;
+  uint8_t *stg = smem + C::OFF_KV + (shared_stg ? C::NREG - 1 : C::NREG - 2 + t) * C::TILE;
+  const uint32_t stg_free = smem_u32(&bars->stg_free);
   const float scale = p.scale_log2;
   uint32_t sc = 0, wgc = 0, lu = 0;
   StoreState<D> ss{0, 0, NSLAB};
@@ -356,29 +387,21 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
       ++sc;
       if (!__all_sync(0xffffffffu, ok)) goto teardown;
       tc_fence_after();
+      // S row in two halves: the max over the first half overlaps the load of
+      // the second.
       uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
-      tmem_wait_ld();
-      // Row max as 8 independent chains, then a tree (short dependency chain).
+      tmem_ld32(tS, s[0]);
+      tmem_ld32(tS + 32, s[1]);
+      tmem_wait_ld_regs(s[0]);
+      tmem_wait_ld_regs(s[1]);
+      tmem_ld32(tS + 64, s[2]);
+      tmem_ld32(tS + 96, s[3]);
       float mp[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        mp[i] = fmaxf(__uint_as_float(s[0][i]), __uint_as_float(s[0][i + 8]));
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        mp[i] = fmaxf(mp[i], fmaxf(__uint_as_float(s[0][i + 16]), __uint_as_float(s[0][i + 24])));
-#pragma unroll
-      for (int c = 1; c < 4; ++c)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mp[i] = fmaxf(mp[i], __uint_as_float(s[c][8 * k + i]));
-#pragma unroll
-      for (int w = 4; w >= 1; w /= 2)
-#pragma unroll
-        for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
-      const float mx = mp[0];
+      row_max_part(s[0], s[1], mp, true);
+      tmem_wait_ld_regs(s[2]);
+      tmem_wait_ld_regs(s[3]);
+      row_max_part(s[2], s[3], mp, false);
+      const float mx = max3(max3(mp[0], mp[1], mp[2]), max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       const float m_new = fmaxf(m, mx * scale);
       // Conditional rescale: keep the running max unless it grew by more than
       // 2^kRescaleThreshold, so O is rescaled only on the rare large jumps.
@@ -396,27 +419,34 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
           }
         }
       }
+      // p = 2^(s*scale - m): the argument on packed pairs, the row sum as four
+      // scalar chains (packing the two MUFU results for a packed add costs more
+      // registers than it saves), P as bf16 pairs over the S columns already read.
       const float neg_m = -m;
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};   // row sum as 4 independent chains
+      const uint64_t scale2 = f2_pack(scale, scale), negm2 = f2_pack(neg_m, neg_m);
+      float lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i]), scale, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i + 1]), scale, neg_m));
-          lp[i % 4] += p0 + p1;
+          const uint64_t x2 = f2_fma(
+              f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])), scale2, negm2);
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          lsum[i & 3] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the S columns already read
+        tmem_st16(tS + 16 * c, pk);
       }
-      l = fmaf(l, alpha, (lp[0] + lp[1]) + (lp[2] + lp[3]));
+      l = fmaf(l, alpha, (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
       if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(tO + 32 * c, o);
@@ -427,20 +457,29 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
       mbar_arrive(p_full);
       // Burst shaping: the previous tile's stores ride on this KV iteration.
       if (elected && ss.next < NSLAB) issue_slabs<D>(p, stg, ss, p.store_tile);
+
     }
     {
       // Epilogue: O_t is final once the last PV MMA completes.
       bool ok = wait_phase(o_full, lu & 1, abort_flag, lim);
       if (!__all_sync(0xffffffffu, ok)) goto teardown;
       tc_fence_after();
-      if (elected) {
-        issue_slabs<D>(p, stg, ss, NSLAB);   // leftovers of the previous tile
-        bulk_wait_read_all();                // staging buffer may be overwritten now
+      if (shared_stg) {
+        // Staging uses alternate between the groups: use k = 2*lu + t waits for
+        // the release of use k - 1.
+        const uint32_t k = 2 * lu + t;
+        ok = k == 0 || wait_phase(stg_free, (k - 1) & 1, abort_flag, lim);
+        if (!__all_sync(0xffffffffu, ok)) goto teardown;
+      } else {
+        if (elected) {
+          issue_slabs<D>(p, stg, ss, NSLAB);   // leftovers of the previous tile
+          bulk_wait_read_all();                // staging buffer may be overwritten now
+        }
+        mbar_arrive(wg_sync);
+        ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
+        ++wgc;
+        if (!__all_sync(0xffffffffu, ok)) goto teardown;
       }
-      mbar_arrive(wg_sync);
-      ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
-      ++wgc;
-      if (!__all_sync(0xffffffffu, ok)) goto teardown;
       if (active) {
         const float inv_l = 1.f / l;
         const int slab = row / kSlabRows, r16 = row % kSlabRows;
@@ -448,7 +487,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(o);
           const int hf = (32 * c) / 64;
           uint8_t *box = stg + (slab * C::NH + hf) * (kSlabRows * 128) + r16 * 128;
 #pragma unroll
@@ -470,6 +509,13 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
       ++wgc;
       if (!__all_sync(0xffffffffu, ok)) goto teardown;
       if (active) ss = StoreState<D>{bh, qtile * BM, 0};
+      if (shared_stg && elected) {
+        // store_tile = 8: the whole tile goes out now, and the staging tile is
+        // handed to the other group as soon as the TMA engine has read it.
+        issue_slabs<D>(p, stg, ss, NSLAB);
+        bulk_wait_read_all();
+        mbar_arrive(stg_free);
+      }
     }
   }
   if (elected) issue_slabs<D>(p, stg, ss, NSLAB);
@@ -477,9 +523,9 @@ teardown:
   if (elected) bulk_wait_all();
 }
 
-template <int D>
+template <int D, bool SHARED>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, SHARED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
@@ -489,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->q_full), 1);
     mbar_init(smem_u32(&bars->q_empty), 1);
-    for (int s = 0; s < C::KV_STAGES; ++s) {
+    for (int s = 0; s < C::MAX_STAGES; ++s) {
       mbar_init(smem_u32(&bars->kv_full[s]), 1);
       mbar_init(smem_u32(&bars->kv_empty[s]), 1);
     }
@@ -500,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(smem_u32(&bars->wg_sync[t]), 128);
     }
     mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->stg_free), 1);
     bars->abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -519,13 +566,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) load_role<D>(p, smem, bars, abort_flag);
+    if (lane == 0) load_role<D, SHARED>(p, smem, bars, abort_flag);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D>(p, smem, bars, tmem, abort_flag);
+    if (lane == 0) mma_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
     __syncwarp();
   } else {
-    softmax_role<D>(p, smem, bars, tmem, abort_flag);
+    softmax_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
   }
 
   tc_fence_before();
@@ -554,22 +601,29 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
 
 }  // namespace
 
-int attn_smem_bytes(int d) { return d == 128 ? Cfg<128>::SMEM : Cfg<64>::SMEM; }
+int attn_smem_bytes(int d) {
+  return d == 128 ? Cfg<128, false>::SMEM : Cfg<64, false>::SMEM;
+}
+
+int attn_kv_stages(int d, bool shared_staging) {
+  if (d == 128) return shared_staging ? Cfg<128, true>::KV_STAGES : Cfg<128, false>::KV_STAGES;
+  return shared_staging ? Cfg<64, true>::KV_STAGES : Cfg<64, false>::KV_STAGES;
+}
+
+template <int D, bool SHARED>
+static cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
+  constexpr int smem = Cfg<D, SHARED>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, SHARED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_kernel<D, SHARED><<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn(const AttnParams &p, int d, int grid, cudaStream_t s) {
-  cudaError_t e;
-  if (d == 128) {
-    e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<128>::SMEM);
-    if (e != cudaSuccess) return e;
-    attn_kernel<128><<<grid, kThreads, Cfg<128>::SMEM, s>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<64>::SMEM);
-    if (e != cudaSuccess) return e;
-    attn_kernel<64><<<grid, kThreads, Cfg<64>::SMEM, s>>>(p);
-  }
-  return cudaGetLastError();
+  const bool shared = p.shared_staging != 0;
+  if (d == 128) return shared ? launch_one<128, true>(p, grid, s) : launch_one<128, false>(p, grid, s);
+  return shared ? launch_one<64, true>(p, grid, s) : launch_one<64, false>(p, grid, s);
 }
 
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {

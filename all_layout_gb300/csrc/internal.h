@@ -20,6 +20,8 @@ struct AttnParams {
   int rows_per_shard;                // N / P
   int shard_mode;                    // 0: o [B][H][N][d] (tm_out[0]); 1: P shards
   int store_tile;                    // slabs issued per KV iteration: 1, 2, 4, 8
+  int shared_staging;                // 1 (store_tile 8): both groups share one staging tile
+  int kv_stages;                     // K/V ring depth, attn_kv_stages(d, shared_staging)
   int n_qtiles;                      // N / 128
   int n_pairs;                       // ceil(n_qtiles / 2): a work unit is a pair of Q tiles
   int n_units;                       // B * H * n_pairs
@@ -33,6 +35,7 @@ struct ShardPtrs {
 };
 
 int attn_smem_bytes(int d);
+int attn_kv_stages(int d, bool shared_staging);
 cudaError_t launch_attn(const AttnParams &p, int d, int grid, cudaStream_t s);
 cudaError_t launch_scatter(const void *o, const ShardPtrs &sh, int B, int N, int H, int d,
                            int rows_per_shard, int grid, cudaStream_t s);
