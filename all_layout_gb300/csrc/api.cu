@@ -99,6 +99,17 @@ bool encode_qkv(CUtensorMap *m, const void *base, int B, int N, int H, int d) {
   return encode(m, const_cast<void *>(base), 3, dims, strides, box);
 }
 
+// A sequence shard [B][rows][H_total][d] as 3-D {d, H_total, B*rows}, box {64, 1, 128}:
+// one box is 128 consecutive rows of one head.
+bool encode_seq_shard(CUtensorMap *m, const void *base, int B, int rows, int H_total, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H_total),
+                              static_cast<cuuint64_t>(B) * rows};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(H_total) * d * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(xs::kTileRows)};
+  return encode(m, const_cast<void *>(base), 3, dims, strides, box);
+}
+
 // Destination rows: 2-D {cols, rows}, row pitch cols*2 bytes, box {64, 16}.
 bool encode_rows(CUtensorMap *m, void *base, unsigned long long cols, unsigned long long rows) {
   const cuuint64_t dims[2] = {cols, rows};
@@ -107,18 +118,40 @@ bool encode_rows(CUtensorMap *m, void *base, unsigned long long cols, unsigned l
   return encode(m, base, 2, dims, strides, box);
 }
 
-xs_status launch_attention(const void *q, const void *k, const void *v, void *o,
-                           void *const *shards, int B, int N, int H, int d, int P, int store_tile,
-                           cudaStream_t stream) {
+// Where the attention inputs come from: head-partition tensors (one pointer each),
+// or P sequence shards per tensor with the computed heads [h0, h0 + H) of H_total.
+struct Inputs {
+  int seq_shards;
+  const void *const *q, *const *k, *const *v;
+  int h0, H_total;
+};
+
+xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B, int N, int H,
+                           int d, int P, int store_tile, cudaStream_t stream) {
   xs::AttnParams prm;
   std::memset(&prm, 0, sizeof(prm));
-  if (!encode_qkv(&prm.tm_q, q, B, N, H, d) || !encode_qkv(&prm.tm_k, k, B, N, H, d) ||
-      !encode_qkv(&prm.tm_v, v, B, N, H, d))
-    return XS_ERR_CUDA;
-  if (shards) {
-    const int R = N / P;
+  const int R = N / P;
+  if (!in.seq_shards) {
+    if (!encode_qkv(&prm.tm_q[0], in.q[0], B, N, H, d) ||
+        !encode_qkv(&prm.tm_k[0], in.k[0], B, N, H, d) ||
+        !encode_qkv(&prm.tm_v[0], in.v[0], B, N, H, d))
+      return XS_ERR_CUDA;
+    prm.in_mode = 0;
+    prm.in_rows = N;
+  } else {
     for (int p = 0; p < P; ++p)
-      if (!encode_rows(&prm.tm_out[p], shards[p], static_cast<unsigned long long>(H) * d,
+      if (!encode_seq_shard(&prm.tm_q[p], in.q[p], B, R, in.H_total, d) ||
+          !encode_seq_shard(&prm.tm_k[p], in.k[p], B, R, in.H_total, d) ||
+          !encode_seq_shard(&prm.tm_v[p], in.v[p], B, R, in.H_total, d))
+        return XS_ERR_CUDA;
+    prm.in_mode = 1;
+    prm.in_rows = R;
+  }
+  prm.h0 = in.h0;
+  prm.H_total = in.H_total;
+  if (shards) {
+    for (int p = 0; p < P; ++p)
+      if (!encode_rows(&prm.tm_out[p], shards[p], static_cast<unsigned long long>(in.H_total) * d,
                        static_cast<unsigned long long>(B) * R))
         return XS_ERR_CUDA;
     prm.shard_mode = 1;
@@ -176,7 +209,8 @@ XS_API xs_status xs_attn_fused(const void *q, const void *k, const void *v,
   const void *ptrs[3] = {q, k, v};
   xs_status st = validate(ptrs, 3, out_shards, B, N, H, d, P, store_tile);
   if (st != XS_OK || empty(B, N, H)) return st;
-  return launch_attention(q, k, v, nullptr, out_shards, B, N, H, d, P, store_tile,
+  const Inputs in{0, &ptrs[0], &ptrs[1], &ptrs[2], 0, H};
+  return launch_attention(in, nullptr, out_shards, B, N, H, d, P, store_tile,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -185,7 +219,8 @@ XS_API xs_status xs_attn(const void *q, const void *k, const void *v, void *o, i
   const void *ptrs[4] = {q, k, v, o};
   xs_status st = validate(ptrs, 4, nullptr, B, N, H, d, 1, 8);
   if (st != XS_OK || empty(B, N, H)) return st;
-  return launch_attention(q, k, v, o, nullptr, B, N, H, d, 1, 8,
+  const Inputs in{0, &ptrs[0], &ptrs[1], &ptrs[2], 0, H};
+  return launch_attention(in, o, nullptr, B, N, H, d, 1, 8,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -206,9 +241,31 @@ XS_API xs_status xs_attn_serial(const void *q, const void *k, const void *v, voi
   xs_status st = validate(ptrs, 4, out_shards, B, N, H, d, P, 8);
   if (st != XS_OK || empty(B, N, H)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = launch_attention(q, k, v, o_scratch, nullptr, B, N, H, d, 1, 8, s);
+  const Inputs in{0, &ptrs[0], &ptrs[1], &ptrs[2], 0, H};
+  st = launch_attention(in, o_scratch, nullptr, B, N, H, d, 1, 8, s);
   if (st != XS_OK) return st;
   return launch_layout(o_scratch, out_shards, B, N, H, d, P, s);
+}
+
+XS_API xs_status xs_attn_ulysses(const void *const *q_shards, const void *const *k_shards,
+                                 const void *const *v_shards, void *const *out_shards, int B,
+                                 int N, int H_total, int h0, int H, int d, int P, int store_tile,
+                                 void *stream) {
+  if (!q_shards || !k_shards || !v_shards || !out_shards) return XS_ERR_INVALID;
+  if (P < 1 || P > xs::kMaxShards) return XS_ERR_INVALID;
+  for (int p = 0; p < P; ++p)
+    if (!q_shards[p] || !k_shards[p] || !v_shards[p]) return XS_ERR_INVALID;
+  if (H_total < 1 || h0 < 0 || H < 0 || h0 + H > H_total) return XS_ERR_INVALID;
+  xs_status st = validate(nullptr, 0, out_shards, B, N, H, d, P, store_tile);
+  if (st != XS_OK) return st;
+  if ((N / P) % xs::kTileRows != 0) return XS_ERR_UNSUPPORTED;
+  for (int p = 0; p < P; ++p)
+    if (!aligned16(q_shards[p]) || !aligned16(k_shards[p]) || !aligned16(v_shards[p]))
+      return XS_ERR_ALIGN;
+  if (empty(B, N, H)) return XS_OK;
+  const Inputs in{1, q_shards, k_shards, v_shards, h0, H_total};
+  return launch_attention(in, nullptr, out_shards, B, N, H, d, P, store_tile,
+                          static_cast<cudaStream_t>(stream));
 }
 
 XS_API const char *xs_status_string(xs_status s) {

@@ -129,6 +129,34 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 // ------------------------------------------------------------------ TMA loader
+// Where the 64-column half `hf` of rows [row0, row0 + 128) of local head-unit bh
+// lives. Head-partition inputs: one map, (x, row, b*H + h). Sequence-shard
+// inputs (the pre-attention All-to-All folded into the load, Figure 5 (a)-(c)):
+// the shard holding row0, (x, h0 + h, b*rows + row0 - shard*rows); 128-row tiles
+// never straddle two shards because rows per shard is a multiple of 128.
+struct TileSrc {
+  const CUtensorMap *m;
+  int x, y, z;
+};
+__device__ __forceinline__ TileSrc tile_src(const AttnParams &p, const CUtensorMap *maps, int hf,
+                                            int row0, int bh) {
+  if (p.in_mode == 0) return TileSrc{&maps[0], hf * 64, row0, bh};
+  const int b = bh / p.H, h = bh - b * p.H;
+  const int sh = row0 / p.in_rows;
+  return TileSrc{&maps[sh], hf * 64, p.h0 + h, b * p.in_rows + (row0 - sh * p.in_rows)};
+}
+__device__ __forceinline__ void load_tile(const AttnParams &p, const CUtensorMap *maps,
+                                          uint32_t dst, uint32_t bar, int hf, int row0, int bh) {
+  const TileSrc t = tile_src(p, maps, hf, row0, bh);
+  tma_load_3d(dst, t.m, bar, t.x, t.y, t.z);
+}
+__device__ __forceinline__ void prefetch_tile(const AttnParams &p, const CUtensorMap *maps, int hf,
+                                              int row0, int bh) {
+  const TileSrc t = tile_src(p, maps, hf, row0, bh);
+  tma_prefetch_l2_3d(t.m, t.x, t.y, t.z);
+}
+
+
 template <int D, bool SHARED>
 __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volatile int *abort_flag) {
   using C = Cfg<D, SHARED>;
@@ -146,9 +174,9 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
     mbar_arrive_expect_tx(q_full, 2 * C::TILE);
     ++q_armed;
     for (int hf = 0; hf < C::NH; ++hf) {
-      tma_load_3d(smem_u32(smem + C::OFF_Q + hf * kHalfBytes), &p.tm_q, q_full, hf * 64, q0a, bh);
-      tma_load_3d(smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), &p.tm_q, q_full, hf * 64,
-                  q0b, bh);
+      load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + hf * kHalfBytes), q_full, hf, q0a, bh);
+      load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), q_full, hf, q0b,
+                bh);
     }
     {
       // Warm L2 with the next unit's query tiles and this unit's first K/V tiles.
@@ -156,31 +184,31 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
       if (un < p.n_units) {
         const int bhn = un / p.n_pairs, pn = un % p.n_pairs;
         for (int hf = 0; hf < C::NH; ++hf) {
-          tma_prefetch_l2_3d(&p.tm_q, hf * 64, pn * 2 * BM, bhn);
-          if (2 * pn + 1 < p.n_qtiles) tma_prefetch_l2_3d(&p.tm_q, hf * 64, pn * 2 * BM + BM, bhn);
+          prefetch_tile(p, p.tm_q, hf, pn * 2 * BM, bhn);
+          if (2 * pn + 1 < p.n_qtiles) prefetch_tile(p, p.tm_q, hf, pn * 2 * BM + BM, bhn);
         }
       }
       for (int j = 0; j < kPrefetchAhead && j < p.n_kv; ++j)
         for (int hf = 0; hf < C::NH; ++hf) {
-          tma_prefetch_l2_3d(&p.tm_k, hf * 64, j * BN, bh);
-          tma_prefetch_l2_3d(&p.tm_v, hf * 64, j * BN, bh);
+          prefetch_tile(p, p.tm_k, hf, j * BN, bh);
+          prefetch_tile(p, p.tm_v, hf, j * BN, bh);
         }
     }
     for (int j = 0; j < p.n_kv; ++j) {
       if (j + kPrefetchAhead < p.n_kv)
         for (int hf = 0; hf < C::NH; ++hf) {
-          tma_prefetch_l2_3d(&p.tm_k, hf * 64, (j + kPrefetchAhead) * BN, bh);
-          tma_prefetch_l2_3d(&p.tm_v, hf * 64, (j + kPrefetchAhead) * BN, bh);
+          prefetch_tile(p, p.tm_k, hf, (j + kPrefetchAhead) * BN, bh);
+          prefetch_tile(p, p.tm_v, hf, (j + kPrefetchAhead) * BN, bh);
         }
       for (int kind = 0; kind < 2; ++kind, ++it) {
         const uint32_t slot = it % stages, ph = (it / stages) & 1;
         if (!wait_phase(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) goto drain;
         const uint32_t full = smem_u32(&bars->kv_full[slot]);
         mbar_arrive_expect_tx(full, C::TILE);
-        const CUtensorMap *m = kind == 0 ? &p.tm_k : &p.tm_v;
+        const CUtensorMap *maps = kind == 0 ? p.tm_k : p.tm_v;
         for (int hf = 0; hf < C::NH; ++hf)
-          tma_load_3d(smem_u32(smem + C::OFF_KV + slot * C::TILE + hf * kHalfBytes), m, full,
-                      hf * 64, j * BN, bh);
+          load_tile(p, maps, smem_u32(smem + C::OFF_KV + slot * C::TILE + hf * kHalfBytes), full,
+                    hf, j * BN, bh);
       }
     }
   }
@@ -323,7 +351,7 @@ __device__ __forceinline__ void issue_slabs(const AttnParams &p, const uint8_t *
       const int sh = n0 / p.rows_per_shard;   // a 16-row slab never straddles two shards
       const int i0 = n0 - sh * p.rows_per_shard;
       m = &p.tm_out[sh];
-      x0 = h * D;
+      x0 = (p.h0 + h) * D;
       y = b * p.rows_per_shard + i0;
     }
 #pragma unroll
@@ -556,9 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     tmem_relinquish();
   }
   if (warp == kLoadWarp && lane == 0) {
-    tma_prefetch_desc(&p.tm_q);
-    tma_prefetch_desc(&p.tm_k);
-    tma_prefetch_desc(&p.tm_v);
+    tma_prefetch_desc(&p.tm_q[0]);
+    tma_prefetch_desc(&p.tm_k[0]);
+    tma_prefetch_desc(&p.tm_v[0]);
   }
   tc_fence_before();
   __syncthreads();

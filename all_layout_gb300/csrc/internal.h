@@ -14,9 +14,15 @@ constexpr int kDevTimeout = 5;
 
 // Everything the attention kernel needs; passed as a __grid_constant__ parameter.
 struct AttnParams {
-  CUtensorMap tm_q, tm_k, tm_v;      // 3-D {d, N, B*H}, box {64, 128, 1}, 128B swizzle
+  // Inputs. in_mode 0: q/k/v [B][H][N][d], one 3-D map each {d, N, B*H}, box {64, 128, 1}.
+  // in_mode 1: P sequence shards [B][N/P][H_total][d] per tensor, 3-D maps
+  // {d, H_total, B*N/P}, box {64, 1, 128}. All with 128-byte swizzle.
+  CUtensorMap tm_q[kMaxShards], tm_k[kMaxShards], tm_v[kMaxShards];
   CUtensorMap tm_out[kMaxShards];    // 2-D destinations, box {64, 16}, 128B swizzle
-  int B, N, H, P;
+  int B, N, H, P;                    // H: heads this call computes
+  int in_mode;                       // 0: head-partition inputs; 1: sequence-shard inputs
+  int in_rows;                       // rows per input sequence shard (in_mode 1)
+  int h0, H_total;                   // global index of local head 0; heads per destination row
   int rows_per_shard;                // N / P
   int shard_mode;                    // 0: o [B][H][N][d] (tm_out[0]); 1: P shards
   int store_tile;                    // slabs issued per KV iteration: 1, 2, 4, 8

@@ -37,8 +37,10 @@ _lib.xs_attn_fused.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _i, _vp]
 _lib.xs_attn.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.xs_scatter.argtypes = [_vp, _PP, _i, _i, _i, _i, _i, _vp]
 _lib.xs_attn_serial.argtypes = [_vp, _vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
+_lib.xs_attn_ulysses.argtypes = [_PP, _PP, _PP, _PP] + [_i] * 8 + [_vp]
 _lib.xs_attn_serial_noalloc.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
 for _f in ("xs_attn_fused", "xs_attn", "xs_scatter", "xs_attn_serial", "xs_attn_serial_noalloc",
+           "xs_attn_ulysses",
            "xs_last_device_status", "xs_selftest_bounded_wait"):
     getattr(_lib, _f).restype = _i
 _lib.xs_status_string.argtypes = [_i]
@@ -131,6 +133,21 @@ def attn_serial(q, k, v, o_scratch, shards, stream=None):
     pp, keep = _shard_array(shards)
     _check(_lib.xs_attn_serial(_ptr(q), _ptr(k), _ptr(v), _ptr(o_scratch), pp, B, N, H, d,
                                len(shards), _stream(stream)), "xs_attn_serial")
+
+
+def attn_ulysses(q_shards, k_shards, v_shards, out_shards, h0, H, store_tile: int = 8,
+                 stream=None):
+    """Both Ulysses All-to-Alls fused: q/k/v_shards are P sequence shards
+    [B, N/P, H_total, d]; computes heads [h0, h0 + H) and stores them into
+    out_shards [B, N/P, H_total, d]."""
+    B, R, H_total, d = (int(x) for x in q_shards[0].shape)
+    P = len(q_shards)
+    qp, kq = _shard_array(q_shards)
+    kp, kk = _shard_array(k_shards)
+    vp, kv = _shard_array(v_shards)
+    op, ko = _shard_array(out_shards)
+    _check(_lib.xs_attn_ulysses(qp, kp, vp, op, B, R * P, H_total, int(h0), int(H), d, P,
+                                int(store_tile), _stream(stream)), "xs_attn_ulysses")
 
 
 def attn_serial_noalloc(q, k, v, shards, stream=None):

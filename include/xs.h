@@ -97,6 +97,32 @@ xs_status xs_attn_serial(const void *q, const void *k, const void *v,
                          void *o_scratch, void *const *out_shards, int B, int N,
                          int H, int d, int P, void *stream);
 
+/* Ulysses sequence-parallel attention with BOTH All-to-Alls fused (Figure 5:
+ * QKV projection and the pre-attention All-to-All turn sequence-partitioned
+ * tokens into head partitions (a)-(c); FlashAttention and the post-attention
+ * All-to-All produce the output and restore the sequence partition (d)-(e)).
+ * The inputs stay in the sequence partition: q_shards[p], k_shards[p],
+ * v_shards[p] (host arrays of P device pointers) are [B][N/P][H_total][d] bf16,
+ * the tokens [p*N/P, (p+1)*N/P) of every head, as each rank holds them after
+ * the QKV projection. The call computes attention over all N tokens for the
+ * heads [h0, h0 + H) only (the head partition one rank owns after the
+ * pre-attention All-to-All), reading its Q/K/V tiles straight from the
+ * sequence shards, and stores output row n of head h0 + h into
+ * out_shards[n / (N/P)][b][n % (N/P)][h0 + h][:] (destinations [B][N/P][H_total][d]),
+ * the owner of each tile issuing the stores as in xs_attn_fused. On one GPU,
+ * h0 = 0 and H = H_total does the whole layer; P calls with
+ * h0 = r*H_total/P, H = H_total/P do rank r's share each.
+ * Validation as xs_attn_fused, plus: XS_ERR_INVALID for NULL arrays or
+ * entries, H_total < 1, h0 < 0, H < 0 or h0 + H > H_total;
+ * XS_ERR_UNSUPPORTED unless N/P is a multiple of 128 (a 128-row tile never
+ * straddles two input shards); XS_ERR_ALIGN for unaligned shard pointers.
+ * H == 0 is an empty call. Heads outside [h0, h0 + H) of the destinations are
+ * not touched. */
+xs_status xs_attn_ulysses(const void *const *q_shards, const void *const *k_shards,
+                          const void *const *v_shards, void *const *out_shards, int B,
+                          int N, int H_total, int h0, int H, int d, int P,
+                          int store_tile, void *stream);
+
 /* Size of the scratch array that xs_attn_serial_noalloc uses: 32 MiB. */
 #define XS_NOALLOC_SCRATCH_BYTES (32ull << 20)
 

@@ -92,3 +92,28 @@ def test_product_path_does_not_import_oracle():
         text = f.read_text()
         assert "import oracle" not in text and "from oracle" not in text, f
         assert "liboracle" not in text, f
+
+
+def _ulysses(xs, q=(A, A), k=(A, A), v=(A, A), out=(A, A), B=1, N=256, Ht=4, h0=0, H=4, d=64,
+             P=None, st=8):
+    lib = xs.library()
+
+    def arr(t):
+        if t is None:
+            return None
+        a = (ctypes.c_void_p * max(1, len(t)))(*t)
+        return ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p))
+    return lib.xs_attn_ulysses(arr(q), arr(k), arr(v), arr(out), B, N, Ht, h0, H, d,
+                               len(out) if P is None else P, st, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(v=(A, None)), 1), (dict(out=(A, None)), 1),
+    (dict(Ht=0, H=0), 1), (dict(h0=-1), 1), (dict(h0=2, H=3), 1), (dict(H=-1), 1),
+    (dict(st=5), 1), (dict(N=384), 2),   # 192-row input shards straddle tiles
+    (dict(d=32), 2), (dict(N=128), 2),
+    (dict(k=(A, A + 8)), 3), (dict(out=(A + 2, A)), 3),
+    (dict(H=0), 0), (dict(B=0), 0),
+])
+def test_ulysses_validation(xs, kw, code):
+    assert _ulysses(xs, **kw) == code

@@ -190,3 +190,44 @@ def test_sweep_points_sampled(xs, idx):
     rows = sample_rows(w.N, w.P, np.random.default_rng(w.seed), extra=8)
     assert_close(gather_rows(got, rows, w.N, w.P), oracle.attention_rows(q, k, v, rows), w.name)
     assert np.all(np.isfinite(got))
+
+
+# ------------------------------------------------------------------ both All-to-Alls fused
+
+def _seq_shards(t, P):
+    """[B, H, N, d] -> P device tensors [B, N/P, H, d] (the sequence partition)."""
+    sh = oracle.shard_layout(inputs.bits(t), P)
+    return [torch.from_numpy(sh[p].view(np.int16)).view(torch.bfloat16).cuda() for p in range(P)]
+
+
+@pytest.mark.parametrize("B,Ht,N,d,P,ranks", [(1, 8, 1024, 128, 4, 4), (2, 6, 768, 64, 3, 3),
+                                              (1, 4, 512, 128, 1, 1), (1, 6, 1024, 128, 2, 3)])
+def test_ulysses_both_all_to_alls(xs, B, Ht, N, d, P, ranks):
+    q, k, v = inputs.qkv(B, N, Ht, d, seed=41 + N + P)
+    qs, ks, vs = _seq_shards(q, P), _seq_shards(k, P), _seq_shards(v, P)
+    out = xs.alloc_shards(B, N, Ht, d, P)
+    for o in out:
+        o.fill_(float("nan"))
+    per = Ht // ranks
+    for r in range(ranks):                      # each "rank" computes its heads
+        xs.attn_ulysses(qs, ks, vs, out, h0=r * per, H=per, store_tile=8 if r % 2 == 0 else 2)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    assert_close(shards_f64(out), ref, "ulysses")
+
+
+def test_ulysses_one_hot_exact_and_untouched_heads(xs):
+    B, Ht, N, d, P = 1, 4, 1024, 128, 4
+    q, k, v, perm = inputs.one_hot_case(B, N, Ht, d, seed=29)
+    qs, ks, vs = _seq_shards(q, P), _seq_shards(k, P), _seq_shards(v, P)
+    out = xs.alloc_shards(B, N, Ht, d, P)
+    for o in out:
+        o.fill_(float("nan"))
+    xs.attn_ulysses(qs, ks, vs, out, h0=1, H=2)          # heads 1 and 2 only
+    torch.cuda.synchronize()
+    vb = inputs.bits(v)
+    exp = oracle.shard_layout(np.take_along_axis(vb, perm[..., None].repeat(d, axis=3), axis=2), P)
+    got = shards_bits(out)
+    assert np.array_equal(got[:, :, :, 1:3], exp[:, :, :, 1:3])
+    assert np.all(np.isnan(shards_f64(out)[:, :, :, [0, 3]]))   # other heads untouched
