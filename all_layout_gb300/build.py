@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libxs.so")
-SOURCES = ("attn.cu", "scatter.cu", "api.cu", "noalloc.cu")
+SOURCES = ("attn.cu", "scatter.cu", "api.cu", "noalloc.cu", "probe.cu")
 HEADERS = (os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"),
            os.path.join(ROOT, "include", "xs.h"))
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

@@ -268,6 +268,24 @@ XS_API xs_status xs_attn_ulysses(const void *const *q_shards, const void *const 
                           static_cast<cudaStream_t>(stream));
 }
 
+XS_API xs_status xs_store_burst_probe(void *dst, unsigned long long dst_bytes, int K,
+                                      unsigned long long burst_bytes, int n_bursts,
+                                      unsigned long long gap_ns, int mode,
+                                      unsigned long long *times, void *stream) {
+  if (!dst || !times || K < 1 || K > 1024 || n_bursts < 1 || (mode != 0 && mode != 1) ||
+      burst_bytes < 2048 || burst_bytes % 2048 != 0 || gap_ns > 1000000000ull)
+    return XS_ERR_INVALID;
+  if (dst_bytes / burst_bytes / static_cast<unsigned long long>(n_bursts) <
+      static_cast<unsigned long long>(K))
+    return XS_ERR_INVALID;
+  if (!aligned16(dst) || (reinterpret_cast<uintptr_t>(times) & 7u) != 0) return XS_ERR_ALIGN;
+  return xs::launch_burst_probe(dst, K, static_cast<long long>(burst_bytes), n_bursts,
+                                static_cast<long long>(gap_ns), mode, times,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? XS_OK
+             : XS_ERR_CUDA;
+}
+
 XS_API const char *xs_status_string(xs_status s) {
   switch (s) {
     case XS_OK: return "ok";

@@ -45,6 +45,9 @@ int attn_kv_stages(int d, bool shared_staging);
 cudaError_t launch_attn(const AttnParams &p, int d, int grid, cudaStream_t s);
 cudaError_t launch_scatter(const void *o, const ShardPtrs &sh, int B, int N, int H, int d,
                            int rows_per_shard, int grid, cudaStream_t s);
+cudaError_t launch_burst_probe(void *dst, int K, long long burst_bytes, int n_bursts,
+                               long long gap_ns, int mode, unsigned long long *times,
+                               cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 cudaError_t read_and_clear_status(cudaStream_t s, int *out);
 

@@ -38,9 +38,11 @@ _lib.xs_attn.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.xs_scatter.argtypes = [_vp, _PP, _i, _i, _i, _i, _i, _vp]
 _lib.xs_attn_serial.argtypes = [_vp, _vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
 _lib.xs_attn_ulysses.argtypes = [_PP, _PP, _PP, _PP] + [_i] * 8 + [_vp]
+_lib.xs_store_burst_probe.argtypes = [_vp, ctypes.c_ulonglong, _i, ctypes.c_ulonglong, _i,
+                                      ctypes.c_ulonglong, _i, _vp, _vp]
 _lib.xs_attn_serial_noalloc.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
 for _f in ("xs_attn_fused", "xs_attn", "xs_scatter", "xs_attn_serial", "xs_attn_serial_noalloc",
-           "xs_attn_ulysses",
+           "xs_attn_ulysses", "xs_store_burst_probe",
            "xs_last_device_status", "xs_selftest_bounded_wait"):
     getattr(_lib, _f).restype = _i
 _lib.xs_status_string.argtypes = [_i]
@@ -157,6 +159,14 @@ def attn_serial_noalloc(q, k, v, shards, stream=None):
     pp, keep = _shard_array(shards)
     _check(_lib.xs_attn_serial_noalloc(_ptr(q), _ptr(k), _ptr(v), pp, B, N, H, d, len(shards),
                                        _stream(stream)), "xs_attn_serial_noalloc")
+
+
+def store_burst_probe(dst, K, burst_bytes, n_bursts, gap_ns, mode, times, stream=None):
+    """Store-burst probe (see xs_store_burst_probe): dst a uint8 CUDA tensor,
+    times an int64 CUDA tensor of 2*K*n_bursts entries."""
+    _check(_lib.xs_store_burst_probe(_ptr(dst), dst.numel() * dst.element_size(), int(K),
+                                     int(burst_bytes), int(n_bursts), int(gap_ns), int(mode),
+                                     _ptr(times), _stream(stream)), "xs_store_burst_probe")
 
 
 def last_device_status(stream=None) -> int:

@@ -123,6 +123,28 @@ xs_status xs_attn_ulysses(const void *const *q_shards, const void *const *k_shar
                           int N, int H_total, int h0, int H, int d, int P,
                           int store_tile, void *stream);
 
+/* Store-burst probe for the Burst-Gap model (Pith review of X-Stage, "What
+ * carries the argument" and "What would settle it": zero-gap periodic bursts
+ * give the drain rate R, a recovered large-gap plateau the backpressure-free
+ * issue time T_iss^0, the isolated-burst knee the outstanding capacity Q;
+ * Figure 3 caption). Local form: the stores go to this GPU's own memory.
+ * K producer CTAs (128 threads each) each issue n_bursts bursts of burst_bytes
+ * into fresh memory, separated by gap_ns nanoseconds without stores. For
+ * producer c and burst b, times[2*(c*n_bursts + b)] and [.. + 1] receive the
+ * %globaltimer values (ns) at which the CTA started issuing the burst and at
+ * which every store had been issued.
+ *   dst       device buffer of dst_bytes >= K*n_bursts*burst_bytes (16-byte aligned)
+ *   times     device buffer of 2*K*n_bursts unsigned 64-bit values (8-byte aligned)
+ *   mode      0: posted st.global.v4 from all threads; 1: TMA bulk copies from
+ *             shared memory, span ending when their source has been read
+ *   XS_ERR_INVALID for NULL pointers, K not in [1, 1024], n_bursts < 1,
+ *   burst_bytes not a positive multiple of 2048, gap_ns > 1e9, a bad mode or a
+ *   too small dst; XS_ERR_ALIGN for misaligned pointers. */
+xs_status xs_store_burst_probe(void *dst, unsigned long long dst_bytes, int K,
+                               unsigned long long burst_bytes, int n_bursts,
+                               unsigned long long gap_ns, int mode,
+                               unsigned long long *times, void *stream);
+
 /* Size of the scratch array that xs_attn_serial_noalloc uses: 32 MiB. */
 #define XS_NOALLOC_SCRATCH_BYTES (32ull << 20)
 
