@@ -127,7 +127,8 @@ struct Inputs {
 };
 
 xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B, int N, int H,
-                           int d, int P, int store_tile, cudaStream_t stream) {
+                           int d, int P, int store_tile, cudaStream_t stream, int coupled = 0,
+                           unsigned long long *spans = nullptr) {
   xs::AttnParams prm;
   std::memset(&prm, 0, sizeof(prm));
   const int R = N / P;
@@ -169,6 +170,8 @@ xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B
   prm.N = N;
   prm.H = H;
   prm.store_tile = store_tile;
+  prm.coupled = coupled;
+  prm.spans = spans;
   prm.shared_staging = store_tile == 8 ? 1 : 0;
   prm.kv_stages = xs::attn_kv_stages(d, store_tile == 8);
   prm.n_qtiles = N / xs::kTileRows;
@@ -212,6 +215,24 @@ XS_API xs_status xs_attn_fused(const void *q, const void *k, const void *v,
   const Inputs in{0, &ptrs[0], &ptrs[1], &ptrs[2], 0, H};
   return launch_attention(in, nullptr, out_shards, B, N, H, d, P, store_tile,
                           static_cast<cudaStream_t>(stream));
+}
+
+XS_API xs_status xs_attn_fused_ex(const void *q, const void *k, const void *v,
+                                  void *const *out_shards, int B, int N, int H, int d, int P,
+                                  int store_tile, int flags, unsigned long long *spans,
+                                  void *stream) {
+  if (!out_shards) return XS_ERR_INVALID;
+  const void *ptrs[3] = {q, k, v};
+  xs_status st = validate(ptrs, 3, out_shards, B, N, H, d, P, store_tile);
+  if (st != XS_OK) return st;
+  if ((flags & ~XS_FLAG_COMPLETION_COUPLED) != 0) return XS_ERR_INVALID;
+  const int coupled = (flags & XS_FLAG_COMPLETION_COUPLED) ? 1 : 0;
+  if (coupled && store_tile != 8) return XS_ERR_INVALID;
+  if (spans && (reinterpret_cast<uintptr_t>(spans) & 7u) != 0) return XS_ERR_ALIGN;
+  if (empty(B, N, H)) return XS_OK;
+  const Inputs in{0, &ptrs[0], &ptrs[1], &ptrs[2], 0, H};
+  return launch_attention(in, nullptr, out_shards, B, N, H, d, P, store_tile,
+                          static_cast<cudaStream_t>(stream), coupled, spans);
 }
 
 XS_API xs_status xs_attn(const void *q, const void *k, const void *v, void *o, int B, int N, int H,

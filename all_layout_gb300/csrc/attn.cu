@@ -75,6 +75,14 @@ struct Cfg {
   static constexpr uint32_t COL_O0 = 256, COL_O1 = 256 + D;
 };
 
+// Store bookkeeping of one warp group, kept in shared memory and touched only by
+// the group's elected thread (keeps registers free for the softmax).
+struct StoreState {
+  int bh, q0, next;   // pending tile and the next slab to issue (NSLAB: nothing pending)
+  int pad;
+  uint64_t t0;        // when the tile's first slab was issued (span recording)
+};
+
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[10], kv_empty[10];
@@ -82,6 +90,7 @@ struct Bars {
   uint64_t wg_sync[2];
   uint64_t drain;
   uint64_t stg_free;   // shared staging tile released (one arrival per use)
+  StoreState store[2];  // per warp group
   uint32_t tmem_base;
   int abort;
 };
@@ -327,40 +336,57 @@ drain:
 }
 
 // ------------------------------------------------------------------ softmax / epilogue
-template <int D>
-struct StoreState {
-  int bh, q0, next;   // pending tile and the next slab to issue (NSLAB: nothing pending)
-};
+// Records an output tile's store-issue span when the caller asked for spans.
+__device__ __forceinline__ void record_span(const AttnParams &p, int bh, int q0, uint64_t t0,
+                                            uint64_t t1) {
+  if (p.spans) {
+    const long long tile = static_cast<long long>(bh) * p.n_qtiles + q0 / BM;
+    p.spans[2 * tile] = t0;
+    p.spans[2 * tile + 1] = t1;
+  }
+}
 
+// One 16-row slab of a staged tile (rows q0 + 16s ... of head unit bh) to its
+// destination: TMA bulk stores of the slab's 64-column halves.
+template <int D>
+__device__ __forceinline__ void issue_slab(const AttnParams &p, const uint8_t *stg, int bh, int q0,
+                                           int s) {
+  constexpr int NH = D / 64;
+  const int n0 = q0 + s * kSlabRows;
+  const CUtensorMap *m;
+  int x0, y;
+  if (p.shard_mode == 0) {
+    m = &p.tm_out[0];
+    x0 = 0;
+    y = bh * p.N + n0;
+  } else {
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int sh = n0 / p.rows_per_shard;   // a 16-row slab never straddles two shards
+    const int i0 = n0 - sh * p.rows_per_shard;
+    m = &p.tm_out[sh];
+    x0 = (p.h0 + h) * D;
+    y = b * p.rows_per_shard + i0;
+  }
+#pragma unroll
+  for (int hf = 0; hf < NH; ++hf)
+    tma_store_2d(m, smem_u32(stg + (s * NH + hf) * (kSlabRows * 128)), x0 + hf * 64, y);
+}
+
+// Issues up to `count` pending slabs of the group's staged tile (deferred bursts).
 template <int D>
 __device__ __forceinline__ void issue_slabs(const AttnParams &p, const uint8_t *stg,
-                                            StoreState<D> &ss, int count) {
-  using C = Cfg<D, false>;
+                                            StoreState &ss, int count) {
   int issued = 0;
+  if (ss.next == 0 && count > 0 && p.spans) ss.t0 = globaltimer_ns();
   while (ss.next < NSLAB && issued < count) {
-    const int s = ss.next;
-    const int n0 = ss.q0 + s * kSlabRows;
-    const CUtensorMap *m;
-    int x0, y;
-    if (p.shard_mode == 0) {
-      m = &p.tm_out[0];
-      x0 = 0;
-      y = ss.bh * p.N + n0;
-    } else {
-      const int b = ss.bh / p.H, h = ss.bh - b * p.H;
-      const int sh = n0 / p.rows_per_shard;   // a 16-row slab never straddles two shards
-      const int i0 = n0 - sh * p.rows_per_shard;
-      m = &p.tm_out[sh];
-      x0 = (p.h0 + h) * D;
-      y = b * p.rows_per_shard + i0;
-    }
-#pragma unroll
-    for (int hf = 0; hf < C::NH; ++hf)
-      tma_store_2d(m, smem_u32(stg + (s * C::NH + hf) * (kSlabRows * 128)), x0 + hf * 64, y);
+    issue_slab<D>(p, stg, ss.bh, ss.q0, ss.next);
     ++ss.next;
     ++issued;
   }
-  if (issued) bulk_commit();
+  if (issued) {
+    bulk_commit();
+    if (ss.next == NSLAB) record_span(p, ss.bh, ss.q0, ss.t0, globaltimer_ns());
+  }
 }
 
 // Running maxima over 64 raw scores (two 32-register chunks) in 8 independent
@@ -403,7 +429,8 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
   const uint32_t stg_free = smem_u32(&bars->stg_free);
   const float scale = p.scale_log2;
   uint32_t sc = 0, wgc = 0, lu = 0;
-  StoreState<D> ss{0, 0, NSLAB};
+  StoreState &ss = bars->store[t];
+  if (elected) ss = StoreState{0, 0, NSLAB, 0, 0};
 
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
     const int bh = u / p.n_pairs, pair = u % p.n_pairs;
@@ -532,23 +559,44 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(wg_sync);
-      ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
-      ++wgc;
-      if (!__all_sync(0xffffffffu, ok)) goto teardown;
-      if (active) ss = StoreState<D>{bh, qtile * BM, 0};
-      if (shared_stg && elected) {
-        // store_tile = 8: the whole tile goes out now, and the staging tile is
-        // handed to the other group as soon as the TMA engine has read it.
-        issue_slabs<D>(p, stg, ss, NSLAB);
-        bulk_wait_read_all();
-        mbar_arrive(stg_free);
+      if (shared_stg) {
+        // store_tile = 8: each warp stores the 32 rows it owns (two slabs) as soon
+        // as they are staged; the staging tile goes to the other group once all
+        // four warps' stores have read it.
+        __syncwarp();
+        if (lane == 0) {
+          if (active) {
+            const uint64_t t0 = p.spans ? globaltimer_ns() : 0;
+            issue_slab<D>(p, stg, bh, qtile * BM, 2 * wq);
+            issue_slab<D>(p, stg, bh, qtile * BM, 2 * wq + 1);
+            bulk_commit();
+            if (p.coupled) {
+              // Counterfactual: the issuer is released only when its stores are complete.
+              bulk_wait_all();
+            } else {
+              bulk_wait_read_all();
+            }
+            if (p.spans) {
+              const long long tile = static_cast<long long>(bh) * p.n_qtiles + qtile;
+              if (wq == 0) p.spans[2 * tile] = t0;
+              atomicMax(&p.spans[2 * tile + 1], static_cast<unsigned long long>(globaltimer_ns()));
+            }
+          }
+          mbar_arrive(stg_free);
+        }
+        __syncwarp();
+      } else {
+        mbar_arrive(wg_sync);
+        ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
+        ++wgc;
+        if (!__all_sync(0xffffffffu, ok)) goto teardown;
+        if (active && elected) ss = StoreState{bh, qtile * BM, 0, 0, 0};
       }
     }
   }
   if (elected) issue_slabs<D>(p, stg, ss, NSLAB);
 teardown:
-  if (elected) bulk_wait_all();
+  if (lane == 0) bulk_wait_all();   // every thread that issued bulk stores
 }
 
 template <int D, bool SHARED>
@@ -574,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(smem_u32(&bars->wg_sync[t]), 128);
     }
     mbar_init(smem_u32(&bars->drain), 1);
-    mbar_init(smem_u32(&bars->stg_free), 1);
+    mbar_init(smem_u32(&bars->stg_free), 4);   // one arrival per warp of a group
     bars->abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();

@@ -33,6 +33,8 @@ struct AttnParams {
   int n_units;                       // B * H * n_pairs
   int n_kv;                          // N / 128
   float scale_log2;                  // log2(e) / sqrt(d)
+  int coupled;                       // 1: the issuer waits for its stores to complete
+  unsigned long long *spans;         // optional: per output tile, store-issue start/end (ns)
   unsigned long long wait_limit_ns;  // bound on every on-chip wait
 };
 

@@ -18,6 +18,7 @@ _HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__)
                        "include", "xs.h")
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT = range(6)
+FLAG_COMPLETION_COUPLED = 1
 MAX_SHARDS = 8
 
 
@@ -34,6 +35,7 @@ _lib = ctypes.CDLL(_LIB_PATH)
 _vp, _i = ctypes.c_void_p, ctypes.c_int
 _PP = ctypes.POINTER(ctypes.c_void_p)
 _lib.xs_attn_fused.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _i, _vp]
+_lib.xs_attn_fused_ex.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _i, _i, _vp, _vp]
 _lib.xs_attn.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
 _lib.xs_scatter.argtypes = [_vp, _PP, _i, _i, _i, _i, _i, _vp]
 _lib.xs_attn_serial.argtypes = [_vp, _vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
@@ -41,7 +43,7 @@ _lib.xs_attn_ulysses.argtypes = [_PP, _PP, _PP, _PP] + [_i] * 8 + [_vp]
 _lib.xs_store_burst_probe.argtypes = [_vp, ctypes.c_ulonglong, _i, ctypes.c_ulonglong, _i,
                                       ctypes.c_ulonglong, _i, _vp, _vp]
 _lib.xs_attn_serial_noalloc.argtypes = [_vp, _vp, _vp, _PP, _i, _i, _i, _i, _i, _vp]
-for _f in ("xs_attn_fused", "xs_attn", "xs_scatter", "xs_attn_serial", "xs_attn_serial_noalloc",
+for _f in ("xs_attn_fused", "xs_attn_fused_ex", "xs_attn", "xs_scatter", "xs_attn_serial", "xs_attn_serial_noalloc",
            "xs_attn_ulysses", "xs_store_burst_probe",
            "xs_last_device_status", "xs_selftest_bounded_wait"):
     getattr(_lib, _f).restype = _i
@@ -113,6 +115,17 @@ def attn_fused(q, k, v, shards, store_tile: int = 8, stream=None):
     pp, keep = _shard_array(shards)
     _check(_lib.xs_attn_fused(_ptr(q), _ptr(k), _ptr(v), pp, B, N, H, d, len(shards),
                               int(store_tile), _stream(stream)), "xs_attn_fused")
+
+
+def attn_fused_ex(q, k, v, shards, store_tile: int = 8, flags: int = 0, spans=None,
+                  stream=None):
+    """xs_attn_fused_ex: optional completion-coupled stores and per-tile store
+    spans (spans: an int64 CUDA tensor of 2*B*H*(N/128) entries, or None)."""
+    B, N, H, d = _dims(q)
+    pp, keep = _shard_array(shards)
+    _check(_lib.xs_attn_fused_ex(_ptr(q), _ptr(k), _ptr(v), pp, B, N, H, d, len(shards),
+                                 int(store_tile), int(flags), _ptr(spans), _stream(stream)),
+           "xs_attn_fused_ex")
 
 
 def attn(q, k, v, o, stream=None):

@@ -78,6 +78,31 @@ xs_status xs_attn_fused(const void *q, const void *k, const void *v,
                         void *const *out_shards, int B, int N, int H, int d,
                         int P, int store_tile, void *stream);
 
+/* Flags of xs_attn_fused_ex. */
+#define XS_FLAG_COMPLETION_COUPLED 1
+
+/* xs_attn_fused with two experiment controls for the residual-slope test
+ * (Pith review of X-Stage, "If this is right": the completion-coupled model,
+ * where the issuer is blocked until its stores are visible, predicts a
+ * residual over FlashAttention alone that grows linearly with sequence length,
+ * while X-Stage predicts a flat one; Figure 11 caption: relative
+ * sender-visible residual E_res(M)/T_FA; referee summary: per-tile
+ * remote-store span distributions).
+ *   flags  0, or XS_FLAG_COMPLETION_COUPLED: after issuing a finished tile's
+ *          stores the issuing thread waits until they have completed before
+ *          its warp group resumes (requires store_tile 8).
+ *   spans  NULL, or a device buffer of 2*B*H*(N/128) unsigned 64-bit values,
+ *          all zero on entry (8-byte aligned): for output tile
+ *          t = (b*H + h)*(N/128) + n/128, spans[2t] and spans[2t + 1] receive
+ *          the %globaltimer (ns) at which its first slab was issued and at which
+ *          the last of its issuing warps was released.
+ * Output bytes are identical to xs_attn_fused. Other flag bits, or the
+ * coupled flag with store_tile != 8: XS_ERR_INVALID. */
+xs_status xs_attn_fused_ex(const void *q, const void *k, const void *v,
+                           void *const *out_shards, int B, int N, int H, int d,
+                           int P, int store_tile, int flags,
+                           unsigned long long *spans, void *stream);
+
 /* Attention alone (the FlashAttention-alone time the abstract compares the
  * fused kernel with): same kernel, output written head-major to
  * o [B][H][N][d] bf16 (device). */

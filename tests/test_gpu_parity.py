@@ -2,6 +2,8 @@
 
 Floating-point outputs must satisfy |err| <= 1e-2 + 1e-2*|ref| elementwise and a
 relative RMS <= 1e-2; placement and the layout kernel must be bit-exact."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -231,3 +233,31 @@ def test_ulysses_one_hot_exact_and_untouched_heads(xs):
     got = shards_bits(out)
     assert np.array_equal(got[:, :, :, 1:3], exp[:, :, :, 1:3])
     assert np.all(np.isnan(shards_f64(out)[:, :, :, [0, 3]]))   # other heads untouched
+
+
+# ------------------------------------------------------------------ experiment controls
+
+@pytest.mark.parametrize("st,flags", [(8, 0), (8, 1), (2, 0)])
+def test_fused_ex_spans_and_coupled_bytes(xs, st, flags):
+    B, H, N, d, P = 1, 3, 1024, 128, 4
+    q, k, v = inputs.qkv(B, N, H, d, seed=61)
+    base = _run_fused(xs, q, k, v, P, 8)
+    out = xs.alloc_shards(B, N, H, d, P)
+    n_tiles = B * H * (N // 128)
+    spans = torch.zeros(2 * n_tiles, dtype=torch.int64, device="cuda")
+    xs.attn_fused_ex(*_dev(q, k, v), out, store_tile=st, flags=flags, spans=spans)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    assert np.array_equal(shards_bits(out), shards_bits(base))      # same bytes as xs_attn_fused
+    t = spans.view(n_tiles, 2).cpu().numpy()
+    assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])          # every tile recorded
+
+
+def test_fused_ex_validation(xs):
+    lib = xs.library()
+    A = 0x10000
+    arr = (ctypes.c_void_p * 2)(A, A)
+    pp = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    assert lib.xs_attn_fused_ex(A, A, A, pp, 1, 256, 4, 64, 2, 8, 2, None, None) == xs.ERR_INVALID
+    assert lib.xs_attn_fused_ex(A, A, A, pp, 1, 256, 4, 64, 2, 4, 1, None, None) == xs.ERR_INVALID
+    assert lib.xs_attn_fused_ex(A, A, A, pp, 1, 256, 4, 64, 2, 8, 0, A + 4, None) == xs.ERR_ALIGN
