@@ -1,0 +1,60 @@
+"""The 96-point sweep: N in {1024, 4096, 16384, 32768} x P in {2, 4, 8} x
+(H, d) in {(24, 128), (48, 64)} x store_tile in {1, 2, 4, 8}, fused vs serial
+(attention then the layout kernel) vs attention alone, one GPU.
+
+Inputs are N(0, 1) bf16 drawn on the device per shape (timing only; the parity
+of sweep points is covered by the GPU tests with the seeded CPU generator).
+L2 is flushed before every timed call. Run as ``python -m all_layout_gb300.sweep``.
+"""
+from __future__ import annotations
+
+import json
+
+import numpy as np
+import torch
+
+from . import inputs, xs
+
+
+def _time_ms(fn, reps, flush):
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return float(np.median(ts))
+
+
+def run(points=None, reps: int = 7):
+    points = points or inputs.sweep_points()
+    flush = torch.empty(128 << 20, dtype=torch.float32, device="cuda")
+    rows, cache = [], {}
+    for w in points:
+        key = (w.N, w.H, w.d)
+        if key not in cache:
+            cache.clear()
+            g = torch.Generator(device="cuda").manual_seed(w.seed)
+            cache[key] = tuple(torch.randn((w.B, w.H, w.N, w.d), device="cuda", generator=g)
+                               .to(torch.bfloat16) for _ in range(3))
+        q, k, v = cache[key]
+        shards = xs.alloc_shards(w.B, w.N, w.H, w.d, w.P)
+        o = torch.empty_like(q)
+        t_f = _time_ms(lambda: xs.attn_fused(q, k, v, shards, w.store_tile), reps, flush)
+        t_s = _time_ms(lambda: xs.attn_serial(q, k, v, o, shards), reps, flush)
+        t_a = _time_ms(lambda: xs.attn(q, k, v, o), reps, flush)
+        rows.append({"N": w.N, "P": w.P, "H": w.H, "d": w.d, "store_tile": w.store_tile,
+                     "t_fused_ms": t_f, "t_serial_ms": t_s, "t_attn_ms": t_a,
+                     "tflops_fused": w.flops / (t_f * 1e-3) / 1e12,
+                     "serial_over_fused": t_s / t_f, "fused_over_attn": t_f / t_a})
+    return rows
+
+
+if __name__ == "__main__":
+    print(json.dumps(run(), indent=1))
