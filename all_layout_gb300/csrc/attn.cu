@@ -105,9 +105,13 @@ __device__ __forceinline__ void record_timeout(volatile int *abort_flag) {
 // aborted or when `limit` ns pass, in which case it records a timeout.
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity,
                                              volatile int *abort_flag, uint64_t limit) {
+  // The MMA issuer polls (it must react to a finished P at once); every other
+  // role sleeps between polls so its waiting costs no issue slots.
+  const bool sleepy = (threadIdx.x / 32) != kMmaWarp;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (sleepy ? mbar_try_wait_sleep(bar, parity, kWaitSleepNs) : mbar_try_wait(bar, parity))
+      return true;
     if ((it & 15u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > limit) {
