@@ -55,6 +55,72 @@ int sm_count() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Caller-owned workspace for the stream-K schedule, one per device (xs_set_workspace).
+struct Workspace {
+  void *ptr;
+  unsigned long long bytes;
+};
+std::mutex g_ws_mu;
+Workspace g_ws[64] = {};
+
+Workspace current_workspace() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Workspace{nullptr, 0};
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  return g_ws[dev];
+}
+
+// Schedule of one launch: whole units strided over `grid` persistent CTAs, or
+// whole units for all but the last full wave followed by a balanced (stream-K)
+// split of the rest into equal contiguous ranges of (unit, KV tile)
+// iterations. The strided waves keep the CTAs on neighbouring units (the same
+// heads' K/V in L2); the stream-K region is at most two waves wide, so its
+// ranges stay within a few neighbouring heads too.
+struct Plan {
+  int sk, sk_waves, grid;
+  unsigned long long bytes;   // workspace the plan needs (0 for whole units)
+};
+
+// Cost model in KV-tile iterations of one CTA: each item adds a fill/drain and
+// epilogue cost, each cut unit a partial write or merge.
+constexpr long kItemCost = 2;
+constexpr long kPieceCost = 3;
+constexpr long kMinPerCta = 4;
+
+unsigned long long sk_bytes(int grid, int d) {
+  return XS_WORKSPACE_HEADER_BYTES +
+         static_cast<unsigned long long>(grid) * 2 * 2 * (d + 2) * xs::kTileRows * 4;
+}
+
+// The stream-K plan when a workspace of `ws_bytes` holds it and the model says
+// it is shorter than whole units; every unit is cut into at most kMaxSplit pieces.
+Plan plan_launch(int units, int sms, int n_kv, int d, unsigned long long ws_bytes) {
+  const int grid0 = units < sms ? units : sms;
+  const Plan whole{0, 0, grid0, 0};
+  if (n_kv < 2 || (units % grid0 == 0 && units >= sms)) return whole;
+  const int waves = units >= sms ? units / sms - 1 : 0;
+  const long long T = static_cast<long long>(units - waves * sms) * n_kv;
+  long long per = (T + sms - 1) / sms, grid = sms;
+  if (waves == 0) {
+    if (per < kMinPerCta) per = kMinPerCta;
+    grid = (T + per - 1) / per;
+    // A unit overlaps at most ceil((n_kv - 1) / shortest range) + 1 ranges.
+    while ((n_kv - 1 + T / grid - 1) / (T / grid) + 1 > xs::kMaxSplit) {
+      ++per;
+      grid = (T + per - 1) / per;
+    }
+  }
+  const long items = static_cast<long>((per + n_kv - 1) / n_kv) + 1;
+  const long cost_sk = waves * (n_kv + kItemCost) + static_cast<long>(per) + items * kItemCost +
+                       2 * kPieceCost;
+  const long cost_whole = static_cast<long>((units + grid0 - 1) / grid0) * (n_kv + kItemCost);
+  const unsigned long long need = sk_bytes(static_cast<int>(grid), d);
+  if (cost_sk >= cost_whole || need > ws_bytes ||
+      static_cast<unsigned long long>(grid) * 2 * 4 * sizeof(int) > XS_WORKSPACE_HEADER_BYTES)
+    return whole;
+  return Plan{1, waves, static_cast<int>(grid), need};
+}
+
 // Validation shared by every entry point, in the order the header states.
 xs_status validate(const void *const *ptrs, int nptrs, void *const *shards, int B, int N, int H,
                    int d, int P, int store_tile) {
@@ -182,7 +248,16 @@ xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B
   prm.wait_limit_ns = g_wait_limit_ns.load();
   const int sms = sm_count();
   if (sms <= 0) return XS_ERR_CUDA;
-  const int grid = prm.n_units < sms ? prm.n_units : sms;
+  const Workspace ws = current_workspace();
+  const Plan pl = plan_launch(prm.n_units, sms, prm.n_kv, d, ws.ptr ? ws.bytes : 0);
+  const int grid = pl.grid;
+  prm.sk = pl.sk;
+  prm.sk_waves = pl.sk_waves;
+  prm.sk_total = static_cast<long long>(prm.n_units - pl.sk_waves * grid) * prm.n_kv;
+  if (pl.sk) {
+    prm.ws_count = static_cast<int *>(ws.ptr);
+    prm.ws_part = reinterpret_cast<float *>(static_cast<char *>(ws.ptr) + XS_WORKSPACE_HEADER_BYTES);
+  }
   return xs::launch_attn(prm, d, grid, stream) == cudaSuccess ? XS_OK : XS_ERR_CUDA;
 }
 
@@ -335,6 +410,40 @@ XS_API xs_status xs_selftest_bounded_wait(void *stream) {
                  cudaSuccess
              ? XS_OK
              : XS_ERR_CUDA;
+}
+
+XS_API xs_status xs_set_workspace(void *ws, unsigned long long bytes, void *stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XS_ERR_CUDA;
+  if (ws) {
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return XS_ERR_ALIGN;
+    if (bytes < XS_WORKSPACE_HEADER_BYTES) return XS_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, XS_WORKSPACE_HEADER_BYTES, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return XS_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  g_ws[dev] = ws ? Workspace{ws, bytes} : Workspace{nullptr, 0};
+  return XS_OK;
+}
+
+XS_API xs_status xs_workspace_bytes(int B, int N, int H, int d, unsigned long long *bytes,
+                                    int *cut) {
+  if (!bytes || B < 0 || N < 0 || H < 0) return XS_ERR_INVALID;
+  if (d != 64 && d != 128) return XS_ERR_UNSUPPORTED;
+  if (N % xs::kTileRows != 0) return XS_ERR_UNSUPPORTED;
+  *bytes = 0;
+  if (cut) *cut = 0;
+  if (empty(B, N, H)) return XS_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return XS_ERR_CUDA;
+  const int n_qtiles = N / xs::kTileRows;
+  const int units = B * H * ((n_qtiles + 1) / 2);
+  const Plan pl = plan_launch(units, sms, n_qtiles, d, ~0ull);
+  *bytes = pl.bytes;
+  if (cut) *cut = pl.sk;
+  return XS_OK;
 }
 
 XS_API int xs_abi_version(void) { return 1; }

@@ -169,6 +169,36 @@ __device__ __forceinline__ void prefetch_tile(const AttnParams &p, const CUtenso
   tma_prefetch_l2_3d(t.m, t.x, t.y, t.z);
 }
 
+// One entry of a CTA's work list: a unit (b*H + h, pair of query tiles) and the
+// KV tiles [kv0, kv1) to process; piece != 0 marks a piece of a cut unit.
+struct Item {
+  int unit, kv0, kv1, piece;
+};
+
+// First iteration of CTA c's stream-K range.
+__device__ __forceinline__ long long sk_start(const AttnParams &p, int c) {
+  return static_cast<long long>(c) * p.sk_total / static_cast<long long>(gridDim.x);
+}
+
+// The k-th item of this CTA's work list; false past its end.
+__device__ __forceinline__ bool get_item(const AttnParams &p, int k, Item &it) {
+  if (!p.sk || k < p.sk_waves) {
+    const int u = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    it = Item{u, 0, p.n_kv, 0};
+    return u < p.n_units;
+  }
+  k -= p.sk_waves;
+  const long long s0 = sk_start(p, blockIdx.x), e0 = sk_start(p, blockIdx.x + 1);
+  const long long pos = k == 0 ? s0 : (s0 / p.n_kv + k) * p.n_kv;
+  if (pos >= e0) return false;
+  const int v = static_cast<int>(pos / p.n_kv);   // unit within the stream-K region
+  const int kv0 = static_cast<int>(pos - static_cast<long long>(v) * p.n_kv);
+  const long long left = e0 - pos;
+  const int kv1 = left < p.n_kv - kv0 ? kv0 + static_cast<int>(left) : p.n_kv;
+  it = Item{p.sk_waves * static_cast<int>(gridDim.x) + v, kv0, kv1,
+            (kv0 > 0 || kv1 < p.n_kv) ? 1 : 0};
+  return true;
+}
 
 template <int D, bool SHARED>
 __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volatile int *abort_flag) {
@@ -179,8 +209,9 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
   uint32_t q_armed = 0;     // q_full phases armed so far
   uint32_t lu = 0;          // units processed by this CTA
   const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
-    const int bh = u / p.n_pairs, pair = u % p.n_pairs;
+  Item item;
+  for (; get_item(p, static_cast<int>(lu), item); ++lu) {
+    const int bh = item.unit / p.n_pairs, pair = item.unit % p.n_pairs;
     const int q0a = pair * 2 * BM;
     const int q0b = (2 * pair + 1 < p.n_qtiles) ? q0a + BM : q0a;  // missing tile: reload tile 0
     if (lu > 0 && !wait_phase(q_empty, (lu - 1) & 1, abort_flag, lim)) goto drain;
@@ -192,23 +223,23 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
                 bh);
     }
     {
-      // Warm L2 with the next unit's query tiles and this unit's first K/V tiles.
-      const int un = u + gridDim.x;
-      if (un < p.n_units) {
-        const int bhn = un / p.n_pairs, pn = un % p.n_pairs;
+      // Warm L2 with the next item's query tiles and this item's first K/V tiles.
+      Item nx;
+      if (get_item(p, static_cast<int>(lu) + 1, nx)) {
+        const int bhn = nx.unit / p.n_pairs, pn = nx.unit % p.n_pairs;
         for (int hf = 0; hf < C::NH; ++hf) {
           prefetch_tile(p, p.tm_q, hf, pn * 2 * BM, bhn);
           if (2 * pn + 1 < p.n_qtiles) prefetch_tile(p, p.tm_q, hf, pn * 2 * BM + BM, bhn);
         }
       }
-      for (int j = 0; j < kPrefetchAhead && j < p.n_kv; ++j)
+      for (int j = item.kv0; j < item.kv0 + kPrefetchAhead && j < item.kv1; ++j)
         for (int hf = 0; hf < C::NH; ++hf) {
           prefetch_tile(p, p.tm_k, hf, j * BN, bh);
           prefetch_tile(p, p.tm_v, hf, j * BN, bh);
         }
     }
-    for (int j = 0; j < p.n_kv; ++j) {
-      if (j + kPrefetchAhead < p.n_kv)
+    for (int j = item.kv0; j < item.kv1; ++j) {
+      if (j + kPrefetchAhead < item.kv1)
         for (int hf = 0; hf < C::NH; ++hf) {
           prefetch_tile(p, p.tm_k, hf, (j + kPrefetchAhead) * BN, bh);
           prefetch_tile(p, p.tm_v, hf, (j + kPrefetchAhead) * BN, bh);
@@ -286,7 +317,9 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
   auto vdesc = [&](uint32_t s) { return vdesc0 + static_cast<uint64_t>(s * (C::TILE >> 4)); };
   const uint32_t col_s[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
   const uint32_t col_o[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
+  Item item;
+  for (; get_item(p, static_cast<int>(lu), item); ++lu) {
+    const int nk = item.kv1 - item.kv0;
     if (!wait_phase(q_full, lu & 1, abort_flag, lim)) goto drain;
     {
       const uint32_t sk = it % stages;
@@ -298,9 +331,9 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
       }
       tc_commit(kv_empty(sk));
       ++it;
-      if (p.n_kv == 1) tc_commit(q_empty);
+      if (nk == 1) tc_commit(q_empty);
     }
-    for (int j = 1; j < p.n_kv; ++j) {
+    for (int j = 1; j < nk; ++j) {
       const uint32_t sv = it % stages, sk = (it + 1) % stages;
       if (!wait_phase(kv_full(sv), (it / stages) & 1, abort_flag, lim)) goto drain;
       for (int t = 0; t < 2; ++t) {
@@ -317,7 +350,7 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
       }
       tc_commit(kv_empty(sk));
       it += 2;
-      if (j == p.n_kv - 1) tc_commit(q_empty);
+      if (j == nk - 1) tc_commit(q_empty);
     }
     {
       const uint32_t sv = it % stages;
@@ -326,7 +359,7 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
         if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
         ++pc[t];
         tc_fence_after();
-        issue_pv<D>(col_o[t], col_s[t], vdesc(sv), p.n_kv > 1 ? 1u : 0u);
+        issue_pv<D>(col_o[t], col_s[t], vdesc(sv), nk > 1 ? 1u : 0u);
         tc_commit(smem_u32(&bars->o_full[t]));
       }
       tc_commit(kv_empty(sv));
@@ -393,6 +426,201 @@ __device__ __forceinline__ void issue_slabs(const AttnParams &p, const uint8_t *
   }
 }
 
+// Writes 32 output columns (chunk c) of one row, scaled by inv_l and rounded to
+// bf16, into the 128B-swizzled staging tile (slab-major, 64-column halves).
+template <int D>
+__device__ __forceinline__ void stage_chunk(uint8_t *stg, int row, int c, const uint32_t (&o)[32],
+                                            float inv_l) {
+  constexpr int NH = D / 64;
+  const int slab = row / kSlabRows, r16 = row % kSlabRows;
+  const int hf = (32 * c) / 64;
+  uint8_t *box = stg + (slab * NH + hf) * (kSlabRows * 128) + r16 * 128;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int chunk = ((32 * c) % 64) / 8 + k;   // 16-byte chunk within the 128-byte row
+    uint4 v;
+    v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+    v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+    v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+    v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+    *reinterpret_cast<uint4 *>(box + ((chunk ^ (r16 & 7)) * 16)) = v;
+  }
+}
+
+// A warp stores the 32 staged rows it owns (slabs 2*wq and 2*wq + 1) and waits
+// until the stores have read the staging tile (or, completion-coupled, until
+// they are complete). Lane 0 only.
+template <int D>
+__device__ __forceinline__ void store_own_rows(const AttnParams &p, const uint8_t *stg, int bh,
+                                               int qtile, int wq) {
+  const uint64_t t0 = p.spans ? globaltimer_ns() : 0;
+  issue_slab<D>(p, stg, bh, qtile * BM, 2 * wq);
+  issue_slab<D>(p, stg, bh, qtile * BM, 2 * wq + 1);
+  bulk_commit();
+  if (p.coupled) {
+    // Counterfactual: the issuer is released only when its stores are complete.
+    bulk_wait_all();
+  } else {
+    bulk_wait_read_all();
+  }
+  if (p.spans) {
+    const long long tile = static_cast<long long>(bh) * p.n_qtiles + qtile;
+    if (wq == 0) p.spans[2 * tile] = t0;
+    atomicMax(&p.spans[2 * tile + 1], static_cast<unsigned long long>(globaltimer_ns()));
+  }
+}
+
+// Partial result of one (piece, query tile) in the workspace, fp32: output
+// columns as float4 groups, [warp][col/4][lane][4] so that one warp instruction
+// moves 512 contiguous bytes, then the running maxima [128] and row sums [128].
+template <int D>
+__device__ __forceinline__ float4 *part_o(float *blk, int wq, int lane, int c4) {
+  return reinterpret_cast<float4 *>(blk) + (wq * (D / 4) + c4) * 32 + lane;
+}
+
+// End of one piece of a split unit, per warp (its 32 rows of query tile t).
+// A piece that is not the last of its unit leaves its partial result
+// (unnormalised O, running maximum m in the log2 domain, row sum l) in the
+// workspace; the warp that completes the last piece of these rows merges all
+// pieces by the same rescaling identity that the online softmax applies
+// between KV tiles, leaving the merged unnormalised O in its Tensor Memory
+// columns and the merged row sum in l, to be staged like a whole unit's.
+// Returns true for that warp.
+template <int D>
+__device__ __forceinline__ bool finish_piece(const AttnParams &p, const Item &item, int t, int wq,
+                                             int lane, int row, uint32_t tO, float m, float &l) {
+  constexpr int BLK = (D + 2) * 128;   // floats of one (piece, tile) partial
+  // The unit's pieces run on the consecutive CTAs whose ranges overlap it.
+  const long long u0 =
+      static_cast<long long>(item.unit - p.sk_waves * static_cast<int>(gridDim.x)) * p.n_kv;
+  auto owner = [&](long long pos) {
+    int c = static_cast<int>(pos * gridDim.x / p.sk_total);
+    while (c + 1 < static_cast<int>(gridDim.x) && sk_start(p, c + 1) <= pos) ++c;
+    while (c > 0 && sk_start(p, c) > pos) --c;
+    return c;
+  };
+  const int c_first = owner(u0);
+  const int S = owner(u0 + p.n_kv - 1) - c_first + 1;
+  const int s_own = static_cast<int>(blockIdx.x) - c_first;
+  // Piece s of the unit lives in CTA c_first + s's slot 1 (the unit starts in
+  // the range of c_first, so it is that CTA's last item) or slot 0 (the first
+  // item of every later CTA).
+  auto part = [&](int k) {
+    return p.ws_part + ((static_cast<size_t>(c_first + k) * 2 + (k == 0 ? 1 : 0)) * 2 + t) * BLK;
+  };
+  int *cnt = p.ws_count + (c_first * 2 + t) * 4 + wq;
+  if (S > kMaxSplit) {   // the host plans at most kMaxSplit pieces per unit
+    if (lane == 0) atomicExch(&g_status, kDevBadPlan);
+    return false;
+  }
+  // Every other piece already counted (each counts after its partial is written
+  // and fenced): this one is last and needs to write nothing. Only piece 0 (the
+  // last item of its CTA's range, usually the last to finish) looks; the later
+  // pieces run first in their CTAs' ranges.
+  int last = 0;
+  if (lane == 0 && s_own == 0) {
+    int seen;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(cnt) : "memory");
+    last = seen == S - 1;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) {
+    float *own = part(s_own);
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + 32 * c, o);
+      tmem_wait_ld_regs(o);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        __stcg(part_o<D>(own, wq, lane, 8 * c + i),
+               make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                           __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3])));
+    }
+    __stcg(own + D * 128 + row, m);
+    __stcg(own + D * 128 + 128 + row, l);
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) last = atomicAdd(cnt, 1) == S - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return false;
+    __threadfence();
+  }
+  if (lane == 0) *cnt = 0;   // every piece has arrived: ready for the next launch
+  // Weights of the pieces relative to the common maximum. Every sum runs over
+  // the pieces in order 0..S-1, so the result does not depend on which piece
+  // finished last.
+  float mk[kMaxSplit], fk[kMaxSplit];
+  float mx = m;
+#pragma unroll
+  for (int k = 0; k < kMaxSplit; ++k) {
+    mk[k] = -INFINITY;
+    if (k < S) mk[k] = k == s_own ? m : __ldcg(part(k) + D * 128 + row);
+    mx = fmaxf(mx, mk[k]);
+  }
+  float lsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxSplit; ++k) {
+    fk[k] = 0.f;
+    if (k < S) {
+      fk[k] = ex2_approx(mk[k] - mx);
+      lsum = fmaf(fk[k], k == s_own ? l : __ldcg(part(k) + D * 128 + 128 + row), lsum);
+    }
+  }
+  // 32 columns of piece k: from Tensor Memory for this piece, else from the workspace.
+  auto fetch = [&](int k, int c, float4 (&x)[8]) {
+    if (k == s_own) {
+      uint32_t o[32];
+      tmem_ld32(tO + 32 * c, o);
+      tmem_wait_ld_regs(o);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        x[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                           __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+    } else if (k < S) {
+#pragma unroll
+      float *src = part(k);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = __ldcg(part_o<D>(src, wq, lane, 8 * c + i));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    // Two pieces' 32 columns in flight at a time.
+#pragma unroll
+    for (int k = 0; k < kMaxSplit; k += 2) {
+      if (k >= S) break;
+      float4 a[8], b[8];
+      fetch(k, c, a);
+      fetch(k + 1, c, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[4 * i + 0] = fmaf(fk[k], a[i].x, acc[4 * i + 0]);
+        acc[4 * i + 1] = fmaf(fk[k], a[i].y, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(fk[k], a[i].z, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(fk[k], a[i].w, acc[4 * i + 3]);
+        acc[4 * i + 0] = fmaf(fk[k + 1], b[i].x, acc[4 * i + 0]);
+        acc[4 * i + 1] = fmaf(fk[k + 1], b[i].y, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(fk[k + 1], b[i].z, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(fk[k + 1], b[i].w, acc[4 * i + 3]);
+      }
+    }
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(acc[i]);
+    tmem_st32(tO + 32 * c, r);
+  }
+  tmem_wait_st();
+  l = lsum;
+  return true;
+}
+
 // Running maxima over 64 raw scores (two 32-register chunks) in 8 independent
 // chains of 3-input max; `first` starts the chains.
 __device__ __forceinline__ void row_max_part(const uint32_t (&a)[32], const uint32_t (&b)[32],
@@ -436,12 +664,14 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
   StoreState &ss = bars->store[t];
   if (elected) ss = StoreState{0, 0, NSLAB, 0, 0};
 
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++lu) {
-    const int bh = u / p.n_pairs, pair = u % p.n_pairs;
+  Item item;
+  for (; get_item(p, static_cast<int>(lu), item); ++lu) {
+    const int bh = item.unit / p.n_pairs, pair = item.unit % p.n_pairs;
     const int qtile = 2 * pair + t;
     const bool active = qtile < p.n_qtiles;
+    const int nk = item.kv1 - item.kv0;
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < p.n_kv; ++j) {
+    for (int j = 0; j < nk; ++j) {
       bool ok = wait_phase(s_full, sc & 1, abort_flag, lim);
       ++sc;
       if (!__all_sync(0xffffffffu, ok)) goto teardown;
@@ -523,11 +753,17 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
       bool ok = wait_phase(o_full, lu & 1, abort_flag, lim);
       if (!__all_sync(0xffffffffu, ok)) goto teardown;
       tc_fence_after();
+      // `mine`: this warp stages and stores its 32 rows of the tile now (always
+      // for a whole unit; for a piece only in the warp that completes the rows,
+      // after merging, which runs before the staging handshake so that the two
+      // groups' merges overlap).
+      bool mine = active;
+      if (active && item.piece) mine = finish_piece<D>(p, item, t, wq, lane, row, tO, m, l);
       if (shared_stg) {
-        // Staging uses alternate between the groups: use k = 2*lu + t waits for
-        // the release of use k - 1.
-        const uint32_t k = 2 * lu + t;
-        ok = k == 0 || wait_phase(stg_free, (k - 1) & 1, abort_flag, lim);
+        // Staging uses alternate between the groups: use 2*lu + t waits for
+        // the release of the use before it.
+        const uint32_t use = 2 * lu + t;
+        ok = use == 0 || wait_phase(stg_free, (use - 1) & 1, abort_flag, lim);
         if (!__all_sync(0xffffffffu, ok)) goto teardown;
       } else {
         if (elected) {
@@ -539,26 +775,14 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         ++wgc;
         if (!__all_sync(0xffffffffu, ok)) goto teardown;
       }
-      if (active) {
+      if (mine) {
         const float inv_l = 1.f / l;
-        const int slab = row / kSlabRows, r16 = row % kSlabRows;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
           tmem_wait_ld_regs(o);
-          const int hf = (32 * c) / 64;
-          uint8_t *box = stg + (slab * C::NH + hf) * (kSlabRows * 128) + r16 * 128;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int chunk = ((32 * c) % 64) / 8 + k;   // 16-byte chunk within the 128-byte row
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-            *reinterpret_cast<uint4 *>(box + ((chunk ^ (r16 & 7)) * 16)) = v;
-          }
+          stage_chunk<D>(stg, row, c, o, inv_l);
         }
         fence_proxy_async_smem();
       }
@@ -569,32 +793,19 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         // four warps' stores have read it.
         __syncwarp();
         if (lane == 0) {
-          if (active) {
-            const uint64_t t0 = p.spans ? globaltimer_ns() : 0;
-            issue_slab<D>(p, stg, bh, qtile * BM, 2 * wq);
-            issue_slab<D>(p, stg, bh, qtile * BM, 2 * wq + 1);
-            bulk_commit();
-            if (p.coupled) {
-              // Counterfactual: the issuer is released only when its stores are complete.
-              bulk_wait_all();
-            } else {
-              bulk_wait_read_all();
-            }
-            if (p.spans) {
-              const long long tile = static_cast<long long>(bh) * p.n_qtiles + qtile;
-              if (wq == 0) p.spans[2 * tile] = t0;
-              atomicMax(&p.spans[2 * tile + 1], static_cast<unsigned long long>(globaltimer_ns()));
-            }
-          }
+          if (mine) store_own_rows<D>(p, stg, bh, qtile, wq);
           mbar_arrive(stg_free);
         }
         __syncwarp();
       } else {
+        // A piece's rows are stored at once (no burst shaping on the split tail).
+        if (item.piece && mine && lane == 0) store_own_rows<D>(p, stg, bh, qtile, wq);
+        __syncwarp();
         mbar_arrive(wg_sync);
         ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
         ++wgc;
         if (!__all_sync(0xffffffffu, ok)) goto teardown;
-        if (active && elected) ss = StoreState{bh, qtile * BM, 0, 0, 0};
+        if (active && elected && !item.piece) ss = StoreState{bh, qtile * BM, 0, 0, 0};
       }
     }
   }

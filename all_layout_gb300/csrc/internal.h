@@ -10,7 +10,9 @@ constexpr int kTileRows = 128;   // query rows per output tile and keys per KV t
 constexpr int kSlabRows = 16;    // rows per store slab (one burst unit)
 
 // Device status codes written by the kernels (same numbers as xs_status).
+constexpr int kMaxSplit = 8;   // pieces per split unit at most
 constexpr int kDevTimeout = 5;
+constexpr int kDevBadPlan = 6;   // a unit cut into more pieces than a merge takes
 
 // Everything the attention kernel needs; passed as a __grid_constant__ parameter.
 struct AttnParams {
@@ -32,6 +34,16 @@ struct AttnParams {
   int n_pairs;                       // ceil(n_qtiles / 2): a work unit is a pair of Q tiles
   int n_units;                       // B * H * n_pairs
   int n_kv;                          // N / 128
+  // Work list of a CTA (G = gridDim.x). sk = 0: whole units u = blockIdx.x + i*G.
+  // sk = 1: first sk_waves whole units the same way (u < sk_waves*G), then
+  // (stream-K) the sk_total = (n_units - sk_waves*G)*n_kv remaining (unit, KV
+  // tile) iterations, unit-major, cut into G contiguous ranges, CTA c taking
+  // [c*sk_total/G, (c+1)*sk_total/G); a unit cut by a range boundary is
+  // finished in pieces whose partial results meet in the workspace.
+  int sk, sk_waves;
+  long long sk_total;
+  float *ws_part;   // sk: partials [G][2 slots][2 tiles][d+2][128] fp32
+  int *ws_count;    // sk: finished pieces per (first CTA of a cut unit, tile, warp)
   float scale_log2;                  // log2(e) / sqrt(d)
   int coupled;                       // 1: the issuer waits for its stores to complete
   unsigned long long *spans;         // optional: per output tile, store-issue start/end (ns)

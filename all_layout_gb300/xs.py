@@ -54,6 +54,11 @@ _lib.xs_selftest_bounded_wait.argtypes = [_vp]
 _lib.xs_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
 _lib.xs_set_wait_limit_ns.restype = ctypes.c_ulonglong
 _lib.xs_abi_version.restype = _i
+_lib.xs_set_workspace.argtypes = [_vp, ctypes.c_ulonglong, _vp]
+_lib.xs_set_workspace.restype = _i
+_lib.xs_workspace_bytes.argtypes = [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong),
+                                    ctypes.POINTER(ctypes.c_int)]
+_lib.xs_workspace_bytes.restype = _i
 
 
 def library():
@@ -198,3 +203,36 @@ def alloc_shards(B, N, H, d, P, device="cuda"):
     """P separate destination buffers [B, N/P, H, d] bf16 (one allocation each)."""
     return [torch.empty((B, N // P, H, d), dtype=torch.bfloat16, device=device)
             for _ in range(P)]
+
+
+def set_workspace(ws=None, stream=None):
+    """Registers a caller-owned uint8 CUDA tensor as the workspace of the
+    balanced (stream-K) schedule on its device (None removes it). Keep the
+    tensor alive while registered."""
+    if ws is None:
+        _check(_lib.xs_set_workspace(None, 0, _stream(stream)), "xs_set_workspace")
+        return
+    if not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    _check(_lib.xs_set_workspace(ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "xs_set_workspace")
+
+
+def workspace_bytes(B: int, N: int, H: int, d: int):
+    """(bytes, cut): the workspace a launch of this shape would use with ample
+    workspace, and 1 if it would take the balanced schedule (else 0)."""
+    b, sp = ctypes.c_ulonglong(0), ctypes.c_int(0)
+    _check(_lib.xs_workspace_bytes(B, N, H, d, ctypes.byref(b), ctypes.byref(sp)),
+           "xs_workspace_bytes")
+    return int(b.value), int(sp.value)
+
+
+def alloc_workspace(B: int, N: int, H: int, d: int, device="cuda"):
+    """Allocates (through torch) and registers the workspace a shape needs;
+    returns the tensor (None when that shape keeps whole units)."""
+    n, _ = workspace_bytes(B, N, H, d)
+    if n == 0:
+        return None
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    set_workspace(ws)
+    return ws

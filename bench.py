@@ -47,6 +47,8 @@ def parse_args():
                     help="steps for the attention-alone / serial / scatter side timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--whole-units", action="store_true",
+                    help="register no workspace: every CTA takes whole units")
     return ap.parse_args()
 
 
@@ -243,6 +245,14 @@ def run_xs(args, w, rank, world, local):
     o = torch.empty_like(q)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # Workspace of the balanced (stream-K) schedule, allocated once before
+    # anything is timed; without it every CTA takes whole units.
+    ws_bytes, cut = xs.workspace_bytes(w.B, w.N, w.H, w.d)
+    workspace = None
+    if args.whole_units or ws_bytes == 0:
+        ws_bytes, cut = 0, 0
+    else:
+        workspace = xs.alloc_workspace(w.B, w.N, w.H, w.d, device=dev)
 
     def fused():
         xs.attn_fused(q, k, v, shards, store_tile=st, stream=stream)
@@ -341,6 +351,8 @@ def run_xs(args, w, rank, world, local):
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "N": w.N, "H": w.H, "d": w.d, "P": w.P,
                        "store_tile": st, "seed": w.seed,
+                       "schedule": "stream-K" if cut else "whole units",
+                       "workspace_bytes": ws_bytes,
                        "l2": "flushed between timed steps (512 MiB write, outside the events)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_peak": 100.0 * achieved / peak,

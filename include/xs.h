@@ -31,7 +31,8 @@
  *    device pointers, read during the call (the array may be freed afterwards).
  *  - Ownership: the caller owns every buffer. The library allocates no device
  *    memory; it keeps only a device status word (see xs_last_device_status)
- *    and the fixed scratch array of xs_attn_serial_noalloc.
+ *    and the fixed scratch array of xs_attn_serial_noalloc. An optional
+ *    caller-owned workspace (xs_set_workspace) enables a balanced schedule.
  *  - Asynchrony: each call only enqueues work on `stream` (a cudaStream_t; NULL
  *    means the legacy default stream) and returns without synchronising. Launch
  *    errors are reported as XS_ERR_CUDA. Kernel-side waits are bounded: a wait
@@ -196,6 +197,48 @@ xs_status xs_store_burst_probe(void *dst, unsigned long long dst_bytes, int K,
 xs_status xs_attn_serial_noalloc(const void *q, const void *k, const void *v,
                                  void *const *out_shards, int B, int N, int H,
                                  int d, int P, void *stream);
+
+/* Balanced schedule with a workspace (a scheduling aid of this implementation;
+ * the paper has no counterpart). The attention kernel runs one persistent CTA
+ * per SM. Without a workspace each CTA takes whole units (a head and a pair of
+ * 128-row query tiles) in turn, so when the units do not divide evenly over
+ * the SMs the last wave leaves SMs idle. With a workspace the launch may
+ * instead give every CTA an equal contiguous range of the (unit, 128-key tile)
+ * iterations (a "stream-K" schedule): a unit cut by a range boundary is
+ * computed in pieces on consecutive CTAs, each piece leaves its partial result
+ * (unnormalised output rows, running maximum, row sum; fp32) in the workspace,
+ * and the CTA finishing a unit's last piece merges the pieces with the
+ * online-softmax rescaling identity and stores the output tile as usual (into
+ * o, or into the shards). The library chooses per launch, from the shape and
+ * the SM count, whichever schedule its cost model finds shorter. Results agree
+ * with the whole-unit schedule within fp32 rounding of the merge (they are not
+ * bit-identical to it) and are identical from launch to launch.
+ *
+ * XS_WORKSPACE_HEADER_BYTES: the first bytes of a workspace hold per-unit
+ * counters that must be zero before a launch; the launches leave them zero. */
+#define XS_WORKSPACE_HEADER_BYTES 16384ull
+
+/* Registers (ws != NULL) or removes (ws == NULL) the caller's device workspace
+ * for the current device. Later attention launches on that device (every entry
+ * point above that computes attention) use it when the balanced schedule is
+ * shorter and `bytes` suffice; otherwise they take whole units. The caller
+ * keeps ownership and must keep the buffer alive until it removes it.
+ *   ws     device memory, 256-byte aligned (XS_ERR_ALIGN otherwise)
+ *   bytes  >= XS_WORKSPACE_HEADER_BYTES (XS_ERR_INVALID otherwise)
+ * The call zeroes the header on `stream` and synchronises it (XS_ERR_CUDA on
+ * failure). Launches that use one workspace must not overlap on the GPU
+ * (different streams without ordering race on it). After a launch reported
+ * XS_ERR_TIMEOUT (xs_last_device_status), register the workspace again to
+ * re-zero its counters. */
+xs_status xs_set_workspace(void *ws, unsigned long long bytes, void *stream);
+
+/* For an attention launch of this shape on the current device with an
+ * unlimited workspace: *bytes = the workspace it would use and *cut = 1 if it
+ * would take the balanced schedule (*bytes = 0 and *cut = 0 for whole units).
+ * cut may be NULL. XS_ERR_INVALID for a NULL bytes or B, N, H < 0;
+ * XS_ERR_UNSUPPORTED for d not in {64, 128} or N % 128 != 0; XS_ERR_CUDA if
+ * the device cannot be queried. */
+xs_status xs_workspace_bytes(int B, int N, int H, int d, unsigned long long *bytes, int *cut);
 
 /* Static English text for a status code; never NULL. */
 const char *xs_status_string(xs_status s);

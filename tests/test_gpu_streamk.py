@@ -1,0 +1,175 @@
+"""Parity of the balanced (stream-K) schedule (xs_set_workspace) with the fp64
+CPU oracle.
+
+With a workspace registered, a launch may give every CTA an equal contiguous
+range of (unit, key tile) iterations; units cut by a range boundary are
+computed in pieces whose partial results are merged on the GPU. The outputs
+must meet the same gates as the whole-unit schedule (|err| <= 1e-2 +
+1e-2*|ref|, relative RMS <= 1e-2), exact placement stays bit-exact, and
+repeated launches give identical bytes (the per-unit counters return to zero)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from all_layout_gb300 import inputs
+from gpu_util import assert_close, gather_rows, sample_rows, shards_bits, shards_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def xs():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    from all_layout_gb300 import xs as _xs
+    torch.cuda.set_device(0)
+    return _xs
+
+
+@pytest.fixture
+def ws(xs):
+    """A 96 MiB workspace registered for the test, removed afterwards."""
+    buf = torch.empty(96 << 20, dtype=torch.uint8, device="cuda")
+    xs.set_workspace(buf)
+    yield buf
+    xs.set_workspace(None)
+
+
+def _dev(*ts):
+    return tuple(t.cuda() for t in ts)
+
+
+def _fused(xs, q, k, v, P, st=8):
+    B, H, N, d = q.shape
+    shards = xs.alloc_shards(B, N, H, d, P)
+    for s in shards:
+        s.fill_(float("nan"))
+    xs.attn_fused(*_dev(q, k, v), shards, store_tile=st)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    return shards
+
+
+def _cut(xs, B, N, H, d):
+    return xs.workspace_bytes(B, N, H, d)[1]
+
+
+# (B, H, N, d, P, q_scale), each taking the balanced schedule on 144..160 SMs:
+# units cut into up to 7 pieces, an odd tile count (the last unit's second
+# tile is empty), one item per CTA, several batches, d = 64, peaked rows.
+SK_SHAPES = [
+    (1, 2, 2944, 128, 2, 1.0),
+    (1, 1, 2816, 64, 4, 1.0),
+    (1, 1, 2048, 128, 2, 4.0),
+    (2, 1, 1664, 128, 4, 2.0),
+    (3, 1, 1792, 64, 7, 1.0),
+    (2, 1, 2944, 64, 1, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,P,qs", SK_SHAPES)
+def test_streamk_shapes_vs_oracle(xs, ws, B, H, N, d, P, qs):
+    assert _cut(xs, B, N, H, d) == 1, "shape chosen to take the balanced schedule"
+    q, k, v = inputs.qkv(B, N, H, d, seed=71 + N + H, q_scale=qs)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    for st in (2, 8):
+        assert_close(shards_f64(_fused(xs, q, k, v, P, st)), ref, f"stream-K st={st}")
+
+
+def test_streamk_image_dit_full(xs, ws):
+    w = inputs.WORKLOADS["image_dit"]
+    assert _cut(xs, w.B, w.N, w.H, w.d) == 1
+    q, k, v = inputs.workload_qkv(w)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), w.P)
+    assert_close(shards_f64(_fused(xs, q, k, v, w.P, w.store_tile)), ref, w.name + " stream-K")
+
+
+@pytest.mark.parametrize("key", ["peaked_16k", "d64"])
+def test_streamk_sampled(xs, ws, key):
+    w = inputs.WORKLOADS["peaked_16k"] if key == "peaked_16k" else \
+        inputs.Workload("d64 B1 N4096 H48", 1, 4096, 48, 64, 8, seed=97)
+    assert _cut(xs, w.B, w.N, w.H, w.d) == 1
+    q, k, v = inputs.workload_qkv(w)
+    got = shards_f64(_fused(xs, q, k, v, w.P, w.store_tile))
+    assert np.all(np.isfinite(got))
+    rows = sample_rows(w.N, w.P, np.random.default_rng(w.seed), extra=8)
+    assert_close(gather_rows(got, rows, w.N, w.P), oracle.attention_rows(q, k, v, rows),
+                 w.name + " stream-K")
+
+
+@pytest.mark.parametrize("B,H,N,d,P", [(1, 2, 2944, 128, 4), (2, 1, 2816, 64, 8)])
+def test_streamk_one_hot_exact(xs, ws, B, H, N, d, P):
+    assert _cut(xs, B, N, H, d) == 1
+    q, k, v, perm = inputs.one_hot_case(B, N, H, d, seed=19)
+    got = shards_bits(_fused(xs, q, k, v, P, 8))
+    o_exp = np.take_along_axis(inputs.bits(v), perm[..., None].repeat(d, axis=3), axis=2)
+    exp = oracle.shard_layout(o_exp, P)
+    if not np.array_equal(got, exp):
+        bad = np.argwhere(got != exp)
+        raise AssertionError(f"{len(bad)} mismatching elements, first at {tuple(bad[0])}")
+
+
+def test_streamk_repeatable_and_fallback(xs):
+    """Two balanced launches in a row give the same bytes; a workspace too small
+    for the schedule (header only) gives the whole-unit bytes; so does none."""
+    B, H, N, d, P = 1, 2, 2944, 128, 2
+    q, k, v = inputs.qkv(B, N, H, d, seed=83)
+    plain = shards_bits(_fused(xs, q, k, v, P))
+    big = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    small = torch.empty(16384, dtype=torch.uint8, device="cuda")
+    try:
+        xs.set_workspace(big)
+        a = shards_bits(_fused(xs, q, k, v, P))
+        b = shards_bits(_fused(xs, q, k, v, P))
+        assert np.array_equal(a, b)
+        assert np.all(big[:16384].cpu().numpy() == 0)       # counters back at zero
+        xs.set_workspace(small)
+        assert np.array_equal(shards_bits(_fused(xs, q, k, v, P)), plain)
+    finally:
+        xs.set_workspace(None)
+    assert np.array_equal(shards_bits(_fused(xs, q, k, v, P)), plain)
+
+
+def test_streamk_attention_alone_serial_and_spans(xs, ws):
+    B, H, N, d, P = 1, 2, 2944, 128, 2
+    q, k, v = inputs.qkv(B, N, H, d, seed=89)
+    qd, kd, vd = _dev(q, k, v)
+    o = torch.empty_like(qd)
+    xs.attn(qd, kd, vd, o)
+    torch.cuda.synchronize()
+    o_ref = oracle.attention(q, k, v)
+    assert_close(o.float().cpu().numpy(), o_ref, "attn stream-K")
+    scratch = torch.empty_like(qd)
+    shards = xs.alloc_shards(B, N, H, d, P)
+    xs.attn_serial(qd, kd, vd, scratch, shards)
+    torch.cuda.synchronize()
+    fused = _fused(xs, q, k, v, P)
+    assert np.array_equal(shards_bits(shards), shards_bits(fused))
+    n_tiles = B * H * (N // 128)
+    for flags in (0, xs.FLAG_COMPLETION_COUPLED):
+        spans = torch.zeros(2 * n_tiles, dtype=torch.int64, device="cuda")
+        out = xs.alloc_shards(B, N, H, d, P)
+        xs.attn_fused_ex(qd, kd, vd, out, store_tile=8, flags=flags, spans=spans)
+        torch.cuda.synchronize()
+        assert xs.last_device_status() == xs.OK
+        assert np.array_equal(shards_bits(out), shards_bits(fused))
+        t = spans.view(n_tiles, 2).cpu().numpy()
+        assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])
+
+
+def test_set_workspace_validation(xs):
+    lib = xs.library()
+    assert lib.xs_set_workspace(ctypes.c_void_p(0x10080), 1 << 20, None) == xs.ERR_ALIGN
+    buf = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    assert lib.xs_set_workspace(ctypes.c_void_p(buf.data_ptr()), 4096, None) == xs.ERR_INVALID
+    assert lib.xs_set_workspace(None, 0, None) == xs.OK
+    n = ctypes.c_ulonglong(7)
+    assert lib.xs_workspace_bytes(1, 1000, 2, 128, ctypes.byref(n), None) == xs.ERR_UNSUPPORTED
+    assert lib.xs_workspace_bytes(1, 1024, 2, 96, ctypes.byref(n), None) == xs.ERR_UNSUPPORTED
+    assert lib.xs_workspace_bytes(1, 1024, 2, 128, None, None) == xs.ERR_INVALID
+    assert lib.xs_workspace_bytes(0, 1024, 2, 128, ctypes.byref(n), None) == xs.OK and n.value == 0
