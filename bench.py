@@ -31,7 +31,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_FILE = os.path.join(ROOT, "profiles", "ncu_attn_fused_image_dit.md")
 KERNEL_SOURCES = ("all_layout_gb300/csrc/attn.cu", "all_layout_gb300/csrc/ptx.cuh",
-                  "all_layout_gb300/csrc/internal.h")
+                  "all_layout_gb300/csrc/internal.h", "all_layout_gb300/csrc/api.cu")
 L2_FLUSH_BYTES = 512 << 20
 
 
