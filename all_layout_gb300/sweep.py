@@ -4,7 +4,10 @@
 
 Inputs are N(0, 1) bf16 drawn on the device per shape (timing only; the parity
 of sweep points is covered by the GPU tests with the seeded CPU generator).
-L2 is flushed before every timed call. Run as ``python -m all_layout_gb300.sweep``.
+L2 is flushed before every timed call. By default a workspace is registered, so
+each shape takes the schedule the library's cost model picks (stream-K or whole
+units). Run as ``python -m all_layout_gb300.sweep`` (``--whole-units`` to
+register none).
 """
 from __future__ import annotations
 
@@ -32,10 +35,18 @@ def _time_ms(fn, reps, flush):
     return float(np.median(ts))
 
 
-def run(points=None, reps: int = 7):
+def run(points=None, reps: int = 7, balanced: bool = True):
+    """Times every point; with `balanced`, a workspace is registered so that each
+    launch may take the stream-K schedule (the same for all three paths)."""
     points = points or inputs.sweep_points()
     flush = torch.empty(128 << 20, dtype=torch.float32, device="cuda")
     rows, cache = [], {}
+    ws = None
+    if balanced:
+        need = max(xs.workspace_bytes(w.B, w.N, w.H, w.d)[0] for w in points)
+        if need:
+            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            xs.set_workspace(ws)
     for w in points:
         key = (w.N, w.H, w.d)
         if key not in cache:
@@ -50,11 +61,15 @@ def run(points=None, reps: int = 7):
         t_s = _time_ms(lambda: xs.attn_serial(q, k, v, o, shards), reps, flush)
         t_a = _time_ms(lambda: xs.attn(q, k, v, o), reps, flush)
         rows.append({"N": w.N, "P": w.P, "H": w.H, "d": w.d, "store_tile": w.store_tile,
+                     "stream_k": int(ws is not None and xs.workspace_bytes(w.B, w.N, w.H, w.d)[1]),
                      "t_fused_ms": t_f, "t_serial_ms": t_s, "t_attn_ms": t_a,
                      "tflops_fused": w.flops / (t_f * 1e-3) / 1e12,
                      "serial_over_fused": t_s / t_f, "fused_over_attn": t_f / t_a})
+    if ws is not None:
+        xs.set_workspace(None)
     return rows
 
 
 if __name__ == "__main__":
-    print(json.dumps(run(), indent=1))
+    import sys
+    print(json.dumps(run(balanced="--whole-units" not in sys.argv), indent=1))
