@@ -53,7 +53,6 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kHalfBytes = BM * 128;     // one 64-column half of a 128-row tile
 constexpr uint32_t kWaitSleepNs = 100000;   // longest suspension per try in a blocked wait
-constexpr int kPrefetchAhead = 4;          // K/V tiles warmed in L2 ahead of their loads
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 template <int D, bool SHARED>
@@ -223,7 +222,9 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
                 bh);
     }
     {
-      // Warm L2 with the next item's query tiles and this item's first K/V tiles.
+      // Warm L2 with the next item's query tiles. K/V tiles are not warmed: the
+      // CTAs of one head read them within a few microseconds of each other, so
+      // they mostly hit in L2, and the extra prefetch requests measured slower.
       Item nx;
       if (get_item(p, static_cast<int>(lu) + 1, nx)) {
         const int bhn = nx.unit / p.n_pairs, pn = nx.unit % p.n_pairs;
@@ -232,18 +233,8 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
           if (2 * pn + 1 < p.n_qtiles) prefetch_tile(p, p.tm_q, hf, pn * 2 * BM + BM, bhn);
         }
       }
-      for (int j = item.kv0; j < item.kv0 + kPrefetchAhead && j < item.kv1; ++j)
-        for (int hf = 0; hf < C::NH; ++hf) {
-          prefetch_tile(p, p.tm_k, hf, j * BN, bh);
-          prefetch_tile(p, p.tm_v, hf, j * BN, bh);
-        }
     }
     for (int j = item.kv0; j < item.kv1; ++j) {
-      if (j + kPrefetchAhead < item.kv1)
-        for (int hf = 0; hf < C::NH; ++hf) {
-          prefetch_tile(p, p.tm_k, hf, (j + kPrefetchAhead) * BN, bh);
-          prefetch_tile(p, p.tm_v, hf, (j + kPrefetchAhead) * BN, bh);
-        }
       for (int kind = 0; kind < 2; ++kind, ++it) {
         const uint32_t slot = it % stages, ph = (it / stages) & 1;
         if (!wait_phase(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) goto drain;
@@ -578,7 +569,6 @@ __device__ __forceinline__ bool finish_piece(const AttnParams &p, const Item &it
         x[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
                            __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
     } else if (k < S) {
-#pragma unroll
       float *src = part(k);
 #pragma unroll
       for (int i = 0; i < 8; ++i) x[i] = __ldcg(part_o<D>(src, wq, lane, 8 * c + i));
