@@ -11,7 +11,10 @@
 // gap absorbs the drain.
 //
 // Work unit: one (batch, head) and a PAIR of 128-row query tiles. A persistent
-// CTA walks units head-major, so a head's K/V stay hot in L2 across CTAs.
+// CTA walks units head-major, so a head's K/V stay hot in L2 across CTAs. With a
+// caller workspace the last waves may instead be cut into equal ranges of
+// (unit, KV tile) iterations (stream-K); a unit cut by a range boundary runs as
+// pieces whose partial results are merged on the GPU (get_item, finish_piece).
 //
 // Roles (320 threads, one CTA per SM):
 //   warps 0-3  softmax warp group 0: owns query tile 0 of the unit (S0, P0, O0)
@@ -20,14 +23,17 @@
 //   warp 9     TMA loader (one thread)
 // Each softmax warp group also rescales its O rows, finalises them, stages the
 // bf16 tile in shared memory and issues the tile's stores to the destination
-// shards as TMA bulk stores, store_tile 16-row slabs after each KV iteration of
-// its next unit. No warp exists only to store.
+// shards as TMA bulk stores: with store_tile = 8 each warp stores its own 32 rows
+// as soon as they are staged; with store_tile < 8, store_tile 16-row slabs go out
+// after each KV iteration of the group's next unit. No warp exists only to store.
 //
 // Tensor Memory (512 columns x 128 lanes, row r of a tile = lane r):
 //   S0 [0,128)  S1 [128,256)  O0 [256,256+d)  O1 [256+d,256+2d)
 //   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
-// Shared memory (d = 128): Q0 Q1 | 3 K/V slots | 2 output staging tiles | barriers,
-// every tile stored as 64-column halves of 128 rows x 128 bytes, 128-byte swizzle.
+// Shared memory (d = 128): Q0 Q1 | five 32 KiB regions: 4 K/V slots + 1 staging
+// tile shared by the two groups (store_tile = 8), or 3 K/V slots + 1 staging tile
+// per group (store_tile < 8) | barriers. Every tile is stored as 64-column halves
+// of 128 rows x 128 bytes, 128-byte swizzle.
 //
 // MMA order per KV step j (t = 0, 1):  O_t += P_t(j-1) V(j-1);  S_t = Q_t K(j)^T.
 // tcgen05 operations issued by one thread execute in order, so S_t(j) cannot
