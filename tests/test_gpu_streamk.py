@@ -173,3 +173,28 @@ def test_set_workspace_validation(xs):
     assert lib.xs_workspace_bytes(1, 1024, 2, 96, ctypes.byref(n), None) == xs.ERR_UNSUPPORTED
     assert lib.xs_workspace_bytes(1, 1024, 2, 128, None, None) == xs.ERR_INVALID
     assert lib.xs_workspace_bytes(0, 1024, 2, 128, ctypes.byref(n), None) == xs.OK and n.value == 0
+
+
+def _seq_shards(t, P):
+    """[B, H, N, d] -> P device tensors [B, N/P, H, d] (the sequence partition)."""
+    sh = oracle.shard_layout(inputs.bits(t), P)
+    return [torch.from_numpy(sh[p].view(np.int16)).view(torch.bfloat16).cuda() for p in range(P)]
+
+
+def test_streamk_ulysses_both_all_to_alls(xs, ws):
+    """Both All-to-Alls fused (inputs read from sequence shards, one call per
+    rank's head share) under the balanced schedule."""
+    B, Ht, N, d, P, ranks = 1, 4, 2816, 128, 2, 2
+    per = Ht // ranks
+    assert _cut(xs, B, N, per, d) == 1
+    q, k, v = inputs.qkv(B, N, Ht, d, seed=101)
+    qs, ks, vs = _seq_shards(q, P), _seq_shards(k, P), _seq_shards(v, P)
+    out = xs.alloc_shards(B, N, Ht, d, P)
+    for o in out:
+        o.fill_(float("nan"))
+    for r in range(ranks):
+        xs.attn_ulysses(qs, ks, vs, out, h0=r * per, H=per, store_tile=8)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    assert_close(shards_f64(out), ref, "ulysses stream-K")
