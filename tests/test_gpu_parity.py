@@ -261,3 +261,40 @@ def test_fused_ex_validation(xs):
     assert lib.xs_attn_fused_ex(A, A, A, pp, 1, 256, 4, 64, 2, 8, 2, None, None) == xs.ERR_INVALID
     assert lib.xs_attn_fused_ex(A, A, A, pp, 1, 256, 4, 64, 2, 4, 1, None, None) == xs.ERR_INVALID
     assert lib.xs_attn_fused_ex(A, A, A, pp, 1, 256, 4, 64, 2, 8, 0, A + 4, None) == xs.ERR_ALIGN
+
+
+# ------------------------------------------------------------------ edge layouts
+
+def test_sixteen_row_shards_exact(xs):
+    """N/P = 16: every 16-row slab of a tile goes to a different destination."""
+    B, H, N, d, P = 2, 3, 128, 128, 8
+    q, k, v, perm = inputs.one_hot_case(B, N, H, d, seed=47)
+    got = shards_bits(_run_fused(xs, q, k, v, P, 8))
+    exp = oracle.shard_layout(np.take_along_axis(inputs.bits(v), perm[..., None].repeat(d, axis=3), axis=2), P)
+    assert np.array_equal(got, exp)
+
+
+def _offset_copy(t, elems):
+    """A device copy of t that starts `elems` bf16 elements into a larger buffer
+    (16-byte aligned for elems % 8 == 0, but not 128-byte aligned)."""
+    buf = torch.empty(t.numel() + elems, dtype=torch.bfloat16, device="cuda")
+    view = buf[elems:].view(t.shape)
+    view.copy_(t.cuda())
+    return view
+
+
+def test_unaligned_to_128_bytes_but_16(xs):
+    """Inputs and destinations at 16-byte (not 128-byte) aligned addresses."""
+    B, H, N, d, P = 4, 2, 512, 64, 4
+    q, k, v = inputs.qkv(B, N, H, d, seed=53)
+    qd, kd, vd = (_offset_copy(t, 8) for t in (q, k, v))
+    assert qd.data_ptr() % 128 == 16
+    shards = []
+    for _ in range(P):
+        sh = _offset_copy(torch.zeros(B, N // P, H, d, dtype=torch.bfloat16), 24)
+        sh.fill_(float("nan"))
+        shards.append(sh)
+    xs.attn_fused(qd, kd, vd, shards, store_tile=2)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    assert_close(shards_f64(shards), oracle.shard_layout(oracle.attention(q, k, v), P), "offset buffers")
