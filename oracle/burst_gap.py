@@ -19,7 +19,7 @@ Communication-Computation Overlap in DiT Inference".
     producers and B = 32 KB per producer, Q(K = 148) ~ 4.25 MiB, sigma ~ 0.79 us
     of Q-loop gap per KV tile, used for the convergence bound M*_ub (Eq. 20).
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
   * completion-coupled issue time = T0 + V/R (issue, then wait for the whole
     burst to drain; the gap does not overlap the drain);
   * Eq. 20 is not printed; M*_ub = block_n * G* / sigma is the reading that
