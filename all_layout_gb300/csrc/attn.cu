@@ -292,17 +292,26 @@ __device__ __forceinline__ void issue_pv(uint32_t dcol, uint32_t pcol, uint64_t 
   }
 }
 
+// Run by the whole MMA warp: the control flow and every descriptor stay
+// warp-uniform, and one elected lane issues each group of tcgen05 operations
+// (the same lane every time, as commits track the issuing thread's MMAs). Kept
+// uniform, the per-MMA descriptor arithmetic stays off the issue path, so the
+// issuer keeps the tensor pipe fed.
 template <int D, bool SHARED>
-__device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem,
+__device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem_in,
                          volatile int *abort_flag) {
   using C = Cfg<D, SHARED>;
   const uint64_t lim = p.wait_limit_ns;
   constexpr uint32_t stages = C::KV_STAGES;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_in, 0);
   uint32_t it = 0, lu = 0;
   uint32_t pc[2] = {0, 0};
   const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
   auto kv_full = [&](uint32_t s) { return smem_u32(&bars->kv_full[s]); };
   auto kv_empty = [&](uint32_t s) { return smem_u32(&bars->kv_empty[s]); };
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, lim));
+  };
   uint64_t qdesc[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t)
@@ -317,55 +326,72 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
   Item item;
   for (; get_item(p, static_cast<int>(lu), item); ++lu) {
     const int nk = item.kv1 - item.kv0;
-    if (!wait_phase(q_full, lu & 1, abort_flag, lim)) goto drain;
+    if (!wait(q_full, lu & 1)) goto drain;
     {
       const uint32_t sk = it % stages;
-      if (!wait_phase(kv_full(sk), (it / stages) & 1, abort_flag, lim)) goto drain;
+      if (!wait(kv_full(sk), (it / stages) & 1)) goto drain;
       tc_fence_after();
-      for (int t = 0; t < 2; ++t) {
-        issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
-        tc_commit(smem_u32(&bars->s_full[t]));
+      if (elect_one()) {
+        for (int t = 0; t < 2; ++t) {
+          issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
+          tc_commit(smem_u32(&bars->s_full[t]));
+        }
+        tc_commit(kv_empty(sk));
+        if (nk == 1) tc_commit(q_empty);
       }
-      tc_commit(kv_empty(sk));
+      __syncwarp();
       ++it;
-      if (nk == 1) tc_commit(q_empty);
     }
     for (int j = 1; j < nk; ++j) {
       const uint32_t sv = it % stages, sk = (it + 1) % stages;
-      if (!wait_phase(kv_full(sv), (it / stages) & 1, abort_flag, lim)) goto drain;
+      if (!wait(kv_full(sv), (it / stages) & 1)) goto drain;
       for (int t = 0; t < 2; ++t) {
-        if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
+        if (!wait(smem_u32(&bars->p_full[t]), pc[t] & 1)) goto drain;
         ++pc[t];
         tc_fence_after();
-        issue_pv<D>(col_o[t], col_s[t], vdesc(sv), j > 1 ? 1u : 0u);
-        if (t == 1) tc_commit(kv_empty(sv));   // V(j-1) is free once PV1 is done
+        if (elect_one()) {
+          issue_pv<D>(col_o[t], col_s[t], vdesc(sv), j > 1 ? 1u : 0u);
+          if (t == 1) tc_commit(kv_empty(sv));   // V(j-1) is free once PV1 is done
+        }
+        __syncwarp();
         // K(j) is needed only now: PV0 above never waits for it.
-        if (t == 0 && !wait_phase(kv_full(sk), ((it + 1) / stages) & 1, abort_flag, lim))
-          goto drain;
-        issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
-        tc_commit(smem_u32(&bars->s_full[t]));
+        if (t == 0) {
+          if (!wait(kv_full(sk), ((it + 1) / stages) & 1)) goto drain;
+          tc_fence_after();
+        }
+        if (elect_one()) {
+          issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
+          tc_commit(smem_u32(&bars->s_full[t]));
+          if (t == 1) {
+            tc_commit(kv_empty(sk));
+            if (j == nk - 1) tc_commit(q_empty);
+          }
+        }
+        __syncwarp();
       }
-      tc_commit(kv_empty(sk));
       it += 2;
-      if (j == nk - 1) tc_commit(q_empty);
     }
     {
       const uint32_t sv = it % stages;
-      if (!wait_phase(kv_full(sv), (it / stages) & 1, abort_flag, lim)) goto drain;
+      if (!wait(kv_full(sv), (it / stages) & 1)) goto drain;
       for (int t = 0; t < 2; ++t) {
-        if (!wait_phase(smem_u32(&bars->p_full[t]), pc[t] & 1, abort_flag, lim)) goto drain;
+        if (!wait(smem_u32(&bars->p_full[t]), pc[t] & 1)) goto drain;
         ++pc[t];
         tc_fence_after();
-        issue_pv<D>(col_o[t], col_s[t], vdesc(sv), nk > 1 ? 1u : 0u);
-        tc_commit(smem_u32(&bars->o_full[t]));
+        if (elect_one()) {
+          issue_pv<D>(col_o[t], col_s[t], vdesc(sv), nk > 1 ? 1u : 0u);
+          tc_commit(smem_u32(&bars->o_full[t]));
+          if (t == 1) tc_commit(kv_empty(sv));
+        }
+        __syncwarp();
       }
-      tc_commit(kv_empty(sv));
       ++it;
     }
   }
 drain:
-  // All MMAs this thread issued must finish before Tensor Memory is released.
-  tc_commit(smem_u32(&bars->drain));
+  // All MMAs this warp issued must finish before Tensor Memory is released.
+  if (elect_one()) tc_commit(smem_u32(&bars->drain));
+  __syncwarp();
   drain_phase(smem_u32(&bars->drain), 0, lim);
 }
 
@@ -856,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (lane == 0) load_role<D, SHARED>(p, smem, bars, abort_flag);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
+    mma_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
     __syncwarp();
   } else {
     softmax_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
