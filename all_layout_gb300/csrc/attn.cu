@@ -19,8 +19,11 @@
 // Roles (320 threads, one CTA per SM):
 //   warps 0-3  softmax warp group 0: owns query tile 0 of the unit (S0, P0, O0)
 //   warps 4-7  softmax warp group 1: owns query tile 1 (S1, P1, O1)
-//   warp 8     MMA issuer (one thread) + Tensor Memory allocation
-//   warp 9     TMA loader (one thread)
+//   warp 8     MMA issuer + Tensor Memory allocation
+//   warp 9     TMA loader
+// The issuer and loader warps run their control flow as whole warps (values stay
+// warp-uniform) and one elected lane issues each group of tcgen05 or TMA
+// operations.
 // Each softmax warp group also rescales its O rows, finalises them, stages the
 // bf16 tile in shared memory and issues the tile's stores to the destination
 // shards as TMA bulk stores: with store_tile = 8 each warp stores its own 32 rows
@@ -214,20 +217,26 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
   uint32_t q_armed = 0;     // q_full phases armed so far
   uint32_t lu = 0;          // units processed by this CTA
   const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, lim));
+  };
   Item item;
   for (; get_item(p, static_cast<int>(lu), item); ++lu) {
     const int bh = item.unit / p.n_pairs, pair = item.unit % p.n_pairs;
     const int q0a = pair * 2 * BM;
     const int q0b = (2 * pair + 1 < p.n_qtiles) ? q0a + BM : q0a;  // missing tile: reload tile 0
-    if (lu > 0 && !wait_phase(q_empty, (lu - 1) & 1, abort_flag, lim)) goto drain;
-    mbar_arrive_expect_tx(q_full, 2 * C::TILE);
-    ++q_armed;
-    for (int hf = 0; hf < C::NH; ++hf) {
-      load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + hf * kHalfBytes), q_full, hf, q0a, bh);
-      load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), q_full, hf, q0b,
-                bh);
+    if (lu > 0 && !wait(q_empty, (lu - 1) & 1)) goto drain;
+    if (elect_one()) {
+      mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+      for (int hf = 0; hf < C::NH; ++hf) {
+        load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + hf * kHalfBytes), q_full, hf, q0a, bh);
+        load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), q_full, hf,
+                  q0b, bh);
+      }
     }
-    {
+    __syncwarp();
+    ++q_armed;
+    if (elect_one()) {
       // Warm L2 with the next item's query tiles. K/V tiles are not warmed: the
       // CTAs of one head read them within a few microseconds of each other, so
       // they mostly hit in L2, and the extra prefetch requests measured slower.
@@ -240,16 +249,20 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
         }
       }
     }
+    __syncwarp();
     for (int j = item.kv0; j < item.kv1; ++j) {
       for (int kind = 0; kind < 2; ++kind, ++it) {
         const uint32_t slot = it % stages, ph = (it / stages) & 1;
-        if (!wait_phase(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) goto drain;
+        if (!wait(smem_u32(&bars->kv_empty[slot]), ph ^ 1)) goto drain;
         const uint32_t full = smem_u32(&bars->kv_full[slot]);
-        mbar_arrive_expect_tx(full, C::TILE);
         const CUtensorMap *maps = kind == 0 ? p.tm_k : p.tm_v;
-        for (int hf = 0; hf < C::NH; ++hf)
-          load_tile(p, maps, smem_u32(smem + C::OFF_KV + slot * C::TILE + hf * kHalfBytes), full,
-                    hf, j * BN, bh);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(full, C::TILE);
+          for (int hf = 0; hf < C::NH; ++hf)
+            load_tile(p, maps, smem_u32(smem + C::OFF_KV + slot * C::TILE + hf * kHalfBytes), full,
+                      hf, j * BN, bh);
+        }
+        __syncwarp();
       }
     }
   }
@@ -879,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) load_role<D, SHARED>(p, smem, bars, abort_flag);
+    load_role<D, SHARED>(p, smem, bars, abort_flag);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     mma_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
