@@ -280,8 +280,7 @@ drain:
 // Descriptors are built once per tile buffer; the k-th MMA of a tile only adds a
 // constant to the start-address field (the low 14 bits hold address >> 4 and
 // shared addresses stay below 256 KiB, so the add never carries out of it).
-// This keeps the single issuing thread's work per MMA to a couple of
-// instructions, so issue never trails the tensor pipe.
+// This keeps the issuing lane's work per MMA to a couple of instructions.
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t dcol, uint64_t qdesc, uint64_t kdesc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0);
