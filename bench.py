@@ -29,7 +29,9 @@ sys.path.insert(0, ROOT)
 METRIC = "fused attn+A2A-layout TFLOP/s & % bf16 peak; fused vs serial time (1 GB300)"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_FILE = os.path.join(ROOT, "profiles", "ncu_attn_fused_image_dit.md")
+# ncu summaries of the fused kernel per workload (store_tile 8, balanced schedule).
+PROFILE_FILES = {"image_dit": os.path.join(ROOT, "profiles", "ncu_attn_fused_image_dit.md"),
+                 "peaked_16k": os.path.join(ROOT, "profiles", "ncu_attn_fused_peaked_16k.md")}
 KERNEL_SOURCES = ("all_layout_gb300/csrc/attn.cu", "all_layout_gb300/csrc/ptx.cuh",
                   "all_layout_gb300/csrc/internal.h", "all_layout_gb300/csrc/api.cu")
 L2_FLUSH_BYTES = 512 << 20
@@ -68,11 +70,15 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    only if it was taken on the current kernel source."""
+def profiled_traffic(workload: str, store_tile: int, balanced: bool):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary of
+    this workload, only if it was taken on the current kernel source and in the
+    launch configuration being timed (store_tile 8, balanced schedule)."""
+    path = PROFILE_FILES.get(workload)
+    if path is None or store_tile != 8 or not balanced:
+        return None
     try:
-        text = open(PROFILE_FILE).read()
+        text = open(path).read()
     except OSError:
         return None
     sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", text)
@@ -372,7 +378,8 @@ def run_xs(args, w, rank, world, local):
     achieved = flops / (ms_per_step * 1e-3) / 1e12        # per launch, this rank's GPU
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_kind": f"{pk_kind} bf16 (burst)",
-                "traffic": profiled_traffic(), "kernel": "attn_kernel<%d> (fused)" % w.d,
+                "traffic": profiled_traffic(args.workload, st, workspace is not None),
+                "kernel": "attn_kernel<%d> (fused)" % w.d,
                 "kernel_sha": kernel_sha()}
 
     cpu = None

@@ -55,3 +55,20 @@ def test_reference_arm_two_ranks_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["steps"] == 3 and rec["unit"] == "TFLOP/s"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_roofline_traffic_only_for_the_profiled_launch():
+    """The bench reports a DRAM traffic figure only for a workload with a committed
+    ncu summary, taken on the current kernel source, in the launch configuration
+    being timed (store_tile 8, balanced schedule); otherwise null."""
+    import re
+    import bench
+    for key, path in bench.PROFILE_FILES.items():
+        text = open(path).read()
+        sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", text).group(1)
+        tb = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text).group(1))
+        want = tb if sha == bench.kernel_sha() else None
+        assert bench.profiled_traffic(key, 8, True) == want
+        assert bench.profiled_traffic(key, 4, True) is None
+        assert bench.profiled_traffic(key, 8, False) is None
+    assert bench.profiled_traffic("video_dit", 8, True) is None
