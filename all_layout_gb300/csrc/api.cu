@@ -267,8 +267,9 @@ xs_status launch_layout(const void *o, void *const *shards, int B, int N, int H,
   for (int p = 0; p < xs::kMaxShards; ++p) sh.p[p] = p < P ? shards[p] : nullptr;
   const int sms = sm_count();
   if (sms <= 0) return XS_ERR_CUDA;
-  const long long vectors = static_cast<long long>(B) * H * N * (d / 8);
-  long long grid = (vectors + 255) / 256;
+  // One warp per 32-row tile, 8 warps per block, at most 8 blocks per SM.
+  const long long tiles = static_cast<long long>(B) * H * N / 32;
+  long long grid = (tiles + 7) / 8;
   if (grid > static_cast<long long>(sms) * 8) grid = static_cast<long long>(sms) * 8;
   if (grid < 1) grid = 1;
   return xs::launch_scatter(o, sh, B, N, H, d, N / P, static_cast<int>(grid), stream) == cudaSuccess

@@ -24,37 +24,40 @@ __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
                : "memory");
 }
 
+// A warp moves tiles of kTileRowsW consecutive rows of one (b, h): one 64-bit
+// division per tile finds b, h and the first row n0, so the per-row index work
+// is one 32-bit division for the shard; all of a tile's loads are in flight
+// before its stores.
+constexpr int kTileRowsW = 32;
+
 template <int D>
 __global__ void __launch_bounds__(256) scatter_kernel(const uint4 *__restrict__ o,
                                                       const __grid_constant__ ShardPtrs sh, int N,
                                                       int H, int R, long long rows_total) {
   constexpr int VPR = D / 8;               // 16-byte vectors per row
   constexpr int RPW = 32 / VPR;            // rows per warp step
-  constexpr int UNROLL = 4;
+  constexpr int STEPS = kTileRowsW / RPW;  // warp steps per tile
   const int lane = threadIdx.x & 31;
   const int sub = lane / VPR, c = lane % VPR;
   const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  const long long step = n_warps * RPW;
-  for (long long base = warp_id * RPW + sub; base < rows_total; base += step * UNROLL) {
-    uint4 v[UNROLL];
+  const long long tiles = rows_total / kTileRowsW;   // N is a multiple of 128
+  for (long long tile = warp_id; tile < tiles; tile += n_warps) {
+    const long long row0 = tile * kTileRowsW;        // row = (b*H + h)*N + n
+    const long long bh = row0 / N;
+    const int n0 = static_cast<int>(row0 - bh * N);
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh - static_cast<long long>(b) * H);
+    const uint4 *src = o + (row0 + sub) * VPR + c;
+    uint4 v[STEPS];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const long long row = base + k * step;
-      if (row < rows_total) v[k] = ld_stream(o + row * VPR + c);
-    }
+    for (int k = 0; k < STEPS; ++k) v[k] = ld_stream(src + k * RPW * VPR);
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const long long row = base + k * step;   // row = (b*H + h)*N + n
-      if (row < rows_total) {
-        const long long bh = row / N;
-        const int n = static_cast<int>(row - bh * N);
-        const int b = static_cast<int>(bh / H), h = static_cast<int>(bh - static_cast<long long>(b) * H);
-        const int p = n / R, i = n - p * R;
-        uint4 *dst = reinterpret_cast<uint4 *>(sh.p[p]) +
-                     ((static_cast<long long>(b) * R + i) * H + h) * VPR + c;
-        st_stream(dst, v[k]);
-      }
+    for (int k = 0; k < STEPS; ++k) {
+      const int n = n0 + k * RPW + sub;
+      const int p = n / R, i = n - p * R;
+      uint4 *dst = reinterpret_cast<uint4 *>(sh.p[p]) +
+                   ((static_cast<long long>(b) * R + i) * H + h) * VPR + c;
+      st_stream(dst, v[k]);
     }
   }
 }
