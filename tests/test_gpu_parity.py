@@ -43,8 +43,12 @@ def _run_fused(xs, q, k, v, P, st=8):
 
 # ------------------------------------------------------------------ layout kernel
 
+# The layout kernel moves tiles of 32 consecutive rows of one (b, h): the last three
+# shapes have shards of 16, 32 and 48 rows, so tiles span two shards or end on a
+# shard boundary.
 @pytest.mark.parametrize("B,H,N,d,P", [(1, 4, 256, 64, 2), (2, 3, 384, 128, 3), (1, 24, 1024, 128, 8),
-                                       (2, 5, 640, 64, 5), (1, 2, 128, 128, 1), (1, 7, 896, 64, 7)])
+                                       (2, 5, 640, 64, 5), (1, 2, 128, 128, 1), (1, 7, 896, 64, 7),
+                                       (2, 3, 128, 128, 8), (1, 3, 256, 64, 8), (3, 2, 384, 64, 8)])
 def test_scatter_bit_exact(xs, B, H, N, d, P):
     o = inputs.tags(B, N, H, d, seed=N + P)
     shards = xs.alloc_shards(B, N, H, d, P)
