@@ -26,17 +26,18 @@
 // operations.
 // Each softmax warp group also rescales its O rows, finalises them, stages the
 // bf16 tile in shared memory and issues the tile's stores to the destination
-// shards as TMA bulk stores: with store_tile = 8 each warp stores its own 32 rows
-// as soon as they are staged; with store_tile < 8, store_tile 16-row slabs go out
-// after each KV iteration of the group's next unit. No warp exists only to store.
+// shards as TMA bulk stores: with store_tile = 8 each warp stages and stores its
+// own 32 rows as two 16-row slabs through a private one-slab buffer; with
+// store_tile < 8, store_tile 16-row slabs go out after each KV iteration of the
+// group's next unit. No warp exists only to store.
 //
 // Tensor Memory (512 columns x 128 lanes, row r of a tile = lane r):
 //   S0 [0,128)  S1 [128,256)  O0 [256,256+d)  O1 [256+d,256+2d)
 //   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
 // Shared memory (d = 128): Q0 Q1 | five 32 KiB regions: 4 K/V slots + 1 staging
-// tile shared by the two groups (store_tile = 8), or 3 K/V slots + 1 staging tile
-// per group (store_tile < 8) | barriers. Every tile is stored as 64-column halves
-// of 128 rows x 128 bytes, 128-byte swizzle.
+// tile cut into eight 4 KiB one-slab buffers, one per softmax warp (store_tile =
+// 8), or 3 K/V slots + 1 staging tile per group (store_tile < 8) | barriers. Every
+// tile is stored as 64-column halves of its rows x 128 bytes, 128-byte swizzle.
 //
 // MMA order per KV step j (t = 0, 1):  O_t += P_t(j-1) V(j-1);  S_t = Q_t K(j)^T.
 // tcgen05 operations issued by one thread execute in order, so S_t(j) cannot
@@ -97,7 +98,6 @@ struct Bars {
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t wg_sync[2];
   uint64_t drain;
-  uint64_t stg_free;   // shared staging tile released (one arrival per use)
   StoreState store[2];  // per warp group
   uint32_t tmem_base;
   int abort;
@@ -448,6 +448,31 @@ __device__ __forceinline__ void issue_slab(const AttnParams &p, const uint8_t *s
     tma_store_2d(m, smem_u32(stg + (s * NH + hf) * (kSlabRows * 128)), x0 + hf * 64, y);
 }
 
+// Slab s of a tile (rows q0 + 16s ...) from a one-slab shared buffer.
+template <int D>
+__device__ __forceinline__ void issue_slab_from(const AttnParams &p, const uint8_t *src, int bh,
+                                                int q0, int s) {
+  constexpr int NH = D / 64;
+  const int n0 = q0 + s * kSlabRows;
+  const CUtensorMap *m;
+  int x0, y;
+  if (p.shard_mode == 0) {
+    m = &p.tm_out[0];
+    x0 = 0;
+    y = bh * p.N + n0;
+  } else {
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int sh = n0 / p.rows_per_shard;
+    const int i0 = n0 - sh * p.rows_per_shard;
+    m = &p.tm_out[sh];
+    x0 = (p.h0 + h) * D;
+    y = b * p.rows_per_shard + i0;
+  }
+#pragma unroll
+  for (int hf = 0; hf < NH; ++hf)
+    tma_store_2d(m, smem_u32(src + hf * (kSlabRows * 128)), x0 + hf * 64, y);
+}
+
 // Issues up to `count` pending slabs of the group's staged tile (deferred bursts).
 template <int D>
 __device__ __forceinline__ void issue_slabs(const AttnParams &p, const uint8_t *stg,
@@ -694,9 +719,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
   const uint32_t tO = tmem + lane_base + (t == 0 ? C::COL_O0 : C::COL_O1);
   const uint32_t s_full = smem_u32(&bars->s_full[t]), p_full = smem_u32(&bars->p_full[t]);
   const uint32_t o_full = smem_u32(&bars->o_full[t]), wg_sync = smem_u32(&bars->wg_sync[t]);
-  constexpr bool shared_stg = SHARED;
-  uint8_t *stg = smem + C::OFF_KV + (shared_stg ? C::NREG - 1 : C::NREG - 2 + t) * C::TILE;
-  const uint32_t stg_free = smem_u32(&bars->stg_free);
+  uint8_t *stg = smem + C::OFF_KV + (SHARED ? C::NREG - 1 : C::NREG - 2 + t) * C::TILE;
   const float scale = p.scale_log2;
   uint32_t sc = 0, wgc = 0, lu = 0;
   StoreState &ss = bars->store[t];
@@ -793,17 +816,50 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
       tc_fence_after();
       // `mine`: this warp stages and stores its 32 rows of the tile now (always
       // for a whole unit; for a piece only in the warp that completes the rows,
-      // after merging, which runs before the staging handshake so that the two
-      // groups' merges overlap).
+      // after merging).
       bool mine = active;
       if (active && item.piece) mine = finish_piece<D>(p, item, t, wq, lane, row, tO, m, l);
-      if (shared_stg) {
-        // Staging uses alternate between the groups: use 2*lu + t waits for
-        // the release of the use before it.
-        const uint32_t use = 2 * lu + t;
-        ok = use == 0 || wait_phase(stg_free, (use - 1) & 1, abort_flag, lim);
-        if (!__all_sync(0xffffffffu, ok)) goto teardown;
+      if constexpr (SHARED) {
+        // store_tile 8: each warp stages and stores its 32 rows as two 16-row
+        // slabs through a private one-slab buffer (its eighth of the staging
+        // tile), so neither group waits for the other's stores, and only the
+        // second slab's buffer read is still pending when the warp moves on.
+        uint8_t *slab_buf = stg + (threadIdx.x / 32) * (kSlabRows * D * 2);
+        if (mine) {
+          const float inv_l = 1.f / l;
+          const uint64_t t0 = p.spans ? globaltimer_ns() : 0;
+          for (int hs = 0; hs < 2; ++hs) {
+            if (lane == 0) bulk_wait_read_all();   // earlier stores have read the buffer
+            __syncwarp();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + 32 * c, o);
+              tmem_wait_ld_regs(o);
+              if ((lane >> 4) == hs) stage_chunk<D>(slab_buf, lane & 15, c, o, inv_l);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              issue_slab_from<D>(p, slab_buf, bh, qtile * BM, 2 * wq + hs);
+              bulk_commit();
+            }
+          }
+          if (lane == 0) {
+            // Counterfactual: the issuer is released only when its stores are complete.
+            if (p.coupled) bulk_wait_all();
+            if (p.spans) {
+              const long long tile = static_cast<long long>(bh) * p.n_qtiles + qtile;
+              if (wq == 0) p.spans[2 * tile] = t0;
+              atomicMax(&p.spans[2 * tile + 1], static_cast<unsigned long long>(globaltimer_ns()));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
       } else {
+        // store_tile < 8: each group keeps its own staging tile; its slabs go
+        // out over the next unit's KV iterations (issue_slabs above).
         if (elected) {
           issue_slabs<D>(p, stg, ss, NSLAB);   // leftovers of the previous tile
           bulk_wait_read_all();                // staging buffer may be overwritten now
@@ -812,38 +868,29 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
         ++wgc;
         if (!__all_sync(0xffffffffu, ok)) goto teardown;
-      }
-      if (mine) {
-        const float inv_l = 1.f / l;
+        if (mine) {
+          const float inv_l = 1.f / l;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_wait_ld_regs(o);
-          stage_chunk<D>(stg, row, c, o, inv_l);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld_regs(o);
+            stage_chunk<D>(stg, row, c, o, inv_l);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      if (shared_stg) {
-        // store_tile = 8: each warp stores the 32 rows it owns (two slabs) as soon
-        // as they are staged; the staging tile goes to the other group once all
-        // four warps' stores have read it.
-        __syncwarp();
-        if (lane == 0) {
-          if (mine) store_own_rows<D>(p, stg, bh, qtile, wq);
-          mbar_arrive(stg_free);
-        }
-        __syncwarp();
-      } else {
-        // A piece's rows are stored at once (no burst shaping on the split tail).
-        if (item.piece && mine && lane == 0) store_own_rows<D>(p, stg, bh, qtile, wq);
+        tc_fence_before();
+        // A piece's rows, and the rows of a CTA's last item (no next unit's KV
+        // iterations to ride on), are stored at once by their owner warps.
+        Item nx;
+        const bool at_once = item.piece || !get_item(p, static_cast<int>(lu) + 1, nx);
+        if (at_once && mine && lane == 0) store_own_rows<D>(p, stg, bh, qtile, wq);
         __syncwarp();
         mbar_arrive(wg_sync);
         ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
         ++wgc;
         if (!__all_sync(0xffffffffu, ok)) goto teardown;
-        if (active && elected && !item.piece) ss = StoreState{bh, qtile * BM, 0, 0, 0};
+        if (active && elected && !at_once) ss = StoreState{bh, qtile * BM, 0, 0, 0};
       }
     }
   }
@@ -875,7 +922,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(smem_u32(&bars->wg_sync[t]), 128);
     }
     mbar_init(smem_u32(&bars->drain), 1);
-    mbar_init(smem_u32(&bars->stg_free), 4);   // one arrival per warp of a group
     bars->abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();

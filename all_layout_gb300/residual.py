@@ -26,20 +26,25 @@ import torch
 from . import xs
 
 
-def _time_ms(fn, reps: int, flush: torch.Tensor) -> float:
-    ts = []
-    for _ in range(3):
-        fn()
+def _time_ms(fns, reps: int, flush: torch.Tensor) -> list:
+    """Median time of each function, the calls interleaved (one of each per
+    round) so that a clock that drifts during the run (the power cap engaging
+    at long N) biases none of them."""
+    ts = [[] for _ in fns]
+    for fn in fns:
+        for _ in range(3):
+            fn()
     torch.cuda.synchronize()
     for _ in range(reps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    return float(np.median(ts))
+        for i, fn in enumerate(fns):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts[i].append(a.elapsed_time(b))
+    return [float(np.median(t)) for t in ts]
 
 
 def measure(N: int, H: int = 24, d: int = 128, P: int = 8, B: int = 1, reps: int = 10,
@@ -50,10 +55,9 @@ def measure(N: int, H: int = 24, d: int = 128, P: int = 8, B: int = 1, reps: int
     shards = xs.alloc_shards(B, N, H, d, P)
     o = torch.empty_like(q)
     flush = torch.empty(128 << 20, dtype=torch.float32, device="cuda")
-    t_attn = _time_ms(lambda: xs.attn(q, k, v, o), reps, flush)
-    t_fused = _time_ms(lambda: xs.attn_fused(q, k, v, shards, 8), reps, flush)
-    t_coupled = _time_ms(lambda: xs.attn_fused_ex(q, k, v, shards, 8, xs.FLAG_COMPLETION_COUPLED),
-                         reps, flush)
+    t_attn, t_fused, t_coupled = _time_ms(
+        [lambda: xs.attn(q, k, v, o), lambda: xs.attn_fused(q, k, v, shards, 8),
+         lambda: xs.attn_fused_ex(q, k, v, shards, 8, xs.FLAG_COMPLETION_COUPLED)], reps, flush)
     n_tiles = B * H * (N // 128)
     spans = {}
     for name, flags in (("fused", 0), ("coupled", xs.FLAG_COMPLETION_COUPLED)):

@@ -19,20 +19,25 @@ import torch
 from . import inputs, xs
 
 
-def _time_ms(fn, reps, flush):
-    for _ in range(2):
-        fn()
+def _time_ms(fns, reps, flush):
+    """Median time of each function, the calls interleaved (one of each per
+    round) so that a clock that drifts during a point (the power cap engaging)
+    biases none of the ratios."""
+    for fn in fns:
+        for _ in range(2):
+            fn()
     torch.cuda.synchronize()
-    ts = []
+    ts = [[] for _ in fns]
     for _ in range(reps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    return float(np.median(ts))
+        for i, fn in enumerate(fns):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts[i].append(a.elapsed_time(b))
+    return [float(np.median(t)) for t in ts]
 
 
 def run(points=None, reps: int = 7, balanced: bool = True):
@@ -57,9 +62,9 @@ def run(points=None, reps: int = 7, balanced: bool = True):
         q, k, v = cache[key]
         shards = xs.alloc_shards(w.B, w.N, w.H, w.d, w.P)
         o = torch.empty_like(q)
-        t_f = _time_ms(lambda: xs.attn_fused(q, k, v, shards, w.store_tile), reps, flush)
-        t_s = _time_ms(lambda: xs.attn_serial(q, k, v, o, shards), reps, flush)
-        t_a = _time_ms(lambda: xs.attn(q, k, v, o), reps, flush)
+        t_f, t_s, t_a = _time_ms([lambda: xs.attn_fused(q, k, v, shards, w.store_tile),
+                                  lambda: xs.attn_serial(q, k, v, o, shards),
+                                  lambda: xs.attn(q, k, v, o)], reps, flush)
         rows.append({"N": w.N, "P": w.P, "H": w.H, "d": w.d, "store_tile": w.store_tile,
                      "stream_k": int(ws is not None and xs.workspace_bytes(w.B, w.N, w.H, w.d)[1]),
                      "t_fused_ms": t_f, "t_serial_ms": t_s, "t_attn_ms": t_a,
