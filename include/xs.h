@@ -70,7 +70,8 @@ typedef enum {
  * kernel. Each finished 128-row output tile is staged on chip and written into
  * the P shards by the warps that own it, in bursts of `store_tile` 16-row slabs
  * interleaved with the KV iterations of that warp group's next tile
- * (store_tile = 8: the whole tile right after it is finished).
+ * (store_tile = 8, or a tile with no next tile on its SM: the whole tile
+ * right after it is finished).
  * The result does not depend on store_tile.
  *   q, k, v     [B][H][N][d] bf16, device.
  *   out_shards  host array of P device pointers, shard p [B][N/P][H][d] bf16.
