@@ -6,6 +6,7 @@ statically; the driver's tensor-map encoder is fetched at run time).
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -21,6 +22,20 @@ HEADERS = (os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"),
            os.path.join(ROOT, "include", "xs.h"))
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden"]
+
+
+# Sources of the attention kernel and its launch path: their hash names the kernel
+# build that a measurement or an ncu summary was taken on.
+KERNEL_SOURCES = ("attn.cu", "ptx.cuh", "internal.h", "api.cu")
+
+
+def kernel_sha() -> str:
+    """First 16 hex digits of the SHA-256 over the kernel sources, in order."""
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(CSRC, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def nvcc() -> str:

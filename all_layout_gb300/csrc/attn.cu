@@ -10,8 +10,10 @@
 // computes. Pith review, "If this is right": a Q-loop longer than the recovery
 // gap absorbs the drain.
 //
-// Work unit: one (batch, head) and a PAIR of 128-row query tiles. A persistent
-// CTA walks units head-major, so a head's K/V stay hot in L2 across CTAs. With a
+// Work unit: one (batch, head) and a PAIR of 128-row query tiles (a single tile
+// for the last unit of a head with an odd tile count: group 1 sits that unit
+// out). A persistent CTA walks units head-major, so a head's K/V stay hot in L2
+// across CTAs. With a
 // caller workspace the last waves may instead be cut into equal ranges of
 // (unit, KV tile) iterations (stream-K); a unit cut by a range boundary runs as
 // pieces whose partial results are merged on the GPU (get_item, finish_piece).
@@ -183,6 +185,12 @@ struct Item {
   int unit, kv0, kv1, piece;
 };
 
+// Query tiles of a unit: 2, or 1 for the last pair of a head with an odd tile
+// count (its second tile would lie past the sequence; nothing computes it).
+__device__ __forceinline__ int unit_tiles(const AttnParams &p, int unit) {
+  return 2 * (unit % p.n_pairs) + 1 < p.n_qtiles ? 2 : 1;
+}
+
 // First iteration of CTA c's stream-K range.
 __device__ __forceinline__ long long sk_start(const AttnParams &p, int c) {
   return static_cast<long long>(c) * p.sk_total / static_cast<long long>(gridDim.x);
@@ -224,14 +232,15 @@ __device__ void load_role(const AttnParams &p, uint8_t *smem, Bars *bars, volati
   for (; get_item(p, static_cast<int>(lu), item); ++lu) {
     const int bh = item.unit / p.n_pairs, pair = item.unit % p.n_pairs;
     const int q0a = pair * 2 * BM;
-    const int q0b = (2 * pair + 1 < p.n_qtiles) ? q0a + BM : q0a;  // missing tile: reload tile 0
+    const int nt = unit_tiles(p, item.unit);
     if (lu > 0 && !wait(q_empty, (lu - 1) & 1)) goto drain;
     if (elect_one()) {
-      mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+      mbar_arrive_expect_tx(q_full, nt * C::TILE);
       for (int hf = 0; hf < C::NH; ++hf) {
         load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + hf * kHalfBytes), q_full, hf, q0a, bh);
-        load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), q_full, hf,
-                  q0b, bh);
+        if (nt == 2)
+          load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + C::TILE + hf * kHalfBytes), q_full, hf,
+                    q0a + BM, bh);
       }
     }
     __syncwarp();
@@ -338,13 +347,14 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
   Item item;
   for (; get_item(p, static_cast<int>(lu), item); ++lu) {
     const int nk = item.kv1 - item.kv0;
+    const int nt = unit_tiles(p, item.unit);   // the last tile's MMAs release K/V and Q
     if (!wait(q_full, lu & 1)) goto drain;
     {
       const uint32_t sk = it % stages;
       if (!wait(kv_full(sk), (it / stages) & 1)) goto drain;
       tc_fence_after();
       if (elect_one()) {
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < nt; ++t) {
           issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
           tc_commit(smem_u32(&bars->s_full[t]));
         }
@@ -362,13 +372,13 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
       // d = 128, K(j) is waited for only after PV0 is issued, which never
       // depends on it).
       if (D == 64 && !wait(kv_full(sk), ((it + 1) / stages) & 1)) goto drain;
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < nt; ++t) {
         if (!wait(smem_u32(&bars->p_full[t]), pc[t] & 1)) goto drain;
         ++pc[t];
         tc_fence_after();
         if (elect_one()) {
           issue_pv<D>(col_o[t], col_s[t], vdesc(sv), j > 1 ? 1u : 0u);
-          if (t == 1) tc_commit(kv_empty(sv));   // V(j-1) is free once PV1 is done
+          if (t == nt - 1) tc_commit(kv_empty(sv));   // V(j-1) is free once the last PV is done
         }
         __syncwarp();
         if (D != 64 && t == 0) {
@@ -378,7 +388,7 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
         if (elect_one()) {
           issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
           tc_commit(smem_u32(&bars->s_full[t]));
-          if (t == 1) {
+          if (t == nt - 1) {
             tc_commit(kv_empty(sk));
             if (j == nk - 1) tc_commit(q_empty);
           }
@@ -390,14 +400,15 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
     {
       const uint32_t sv = it % stages;
       if (!wait(kv_full(sv), (it / stages) & 1)) goto drain;
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < nt; ++t) {
         if (!wait(smem_u32(&bars->p_full[t]), pc[t] & 1)) goto drain;
         ++pc[t];
         tc_fence_after();
         if (elect_one()) {
           issue_pv<D>(col_o[t], col_s[t], vdesc(sv), nk > 1 ? 1u : 0u);
           tc_commit(smem_u32(&bars->o_full[t]));
-          if (t == 1) tc_commit(kv_empty(sv));
+          if (t == nt - 1) tc_commit(kv_empty(sv));
+          if (nt == 1) tc_commit(smem_u32(&bars->o_full[1]));   // group 1 sits this unit out
         }
         __syncwarp();
       }
@@ -420,6 +431,20 @@ __device__ __forceinline__ void record_span(const AttnParams &p, int bh, int q0,
     p.spans[2 * tile] = t0;
     p.spans[2 * tile + 1] = t1;
   }
+}
+
+// One of the warps that store a tile's rows: the span runs from the earliest
+// first issue to the latest release over all of them (they may sit in different
+// CTAs when the tile was cut into pieces). The entries start at zero and timer
+// values are positive, so the first warp's start replaces the zero and every
+// later one keeps the minimum.
+__device__ __forceinline__ void record_span_part(const AttnParams &p, int bh, int qtile,
+                                                 uint64_t t0, uint64_t t1) {
+  const long long tile = static_cast<long long>(bh) * p.n_qtiles + qtile;
+  unsigned long long *s = p.spans + 2 * tile;
+  const unsigned long long seen = atomicCAS(s, 0ull, static_cast<unsigned long long>(t0));
+  if (seen != 0ull && t0 < seen) atomicMin(s, static_cast<unsigned long long>(t0));
+  atomicMax(s + 1, static_cast<unsigned long long>(t1));
 }
 
 // One 16-row slab of a staged tile (rows q0 + 16s ... of head unit bh) to its
@@ -527,11 +552,7 @@ __device__ __forceinline__ void store_own_rows(const AttnParams &p, const uint8_
   } else {
     bulk_wait_read_all();
   }
-  if (p.spans) {
-    const long long tile = static_cast<long long>(bh) * p.n_qtiles + qtile;
-    if (wq == 0) p.spans[2 * tile] = t0;
-    atomicMax(&p.spans[2 * tile + 1], static_cast<unsigned long long>(globaltimer_ns()));
-  }
+  if (p.spans) record_span_part(p, bh, qtile, t0, globaltimer_ns());
 }
 
 // Partial result of one (piece, query tile) in the workspace, fp32: output
@@ -729,7 +750,13 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
   for (; get_item(p, static_cast<int>(lu), item); ++lu) {
     const int bh = item.unit / p.n_pairs, pair = item.unit % p.n_pairs;
     const int qtile = 2 * pair + t;
-    const bool active = qtile < p.n_qtiles;
+    // A unit with one query tile leaves group 1 nothing to compute: the issuer
+    // runs no MMA for it and only completes the group's o_full phase (so the
+    // phases stay one per item), which the group consumes and moves on.
+    if (t >= unit_tiles(p, item.unit)) {
+      if (!__all_sync(0xffffffffu, wait_phase(o_full, lu & 1, abort_flag, lim))) goto teardown;
+      continue;
+    }
     const int nk = item.kv1 - item.kv0;
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < nk; ++j) {
@@ -817,8 +844,8 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
       // `mine`: this warp stages and stores its 32 rows of the tile now (always
       // for a whole unit; for a piece only in the warp that completes the rows,
       // after merging).
-      bool mine = active;
-      if (active && item.piece) mine = finish_piece<D>(p, item, t, wq, lane, row, tO, m, l);
+      bool mine = true;
+      if (item.piece) mine = finish_piece<D>(p, item, t, wq, lane, row, tO, m, l);
       if constexpr (SHARED) {
         // store_tile 8: each warp stages and stores its 32 rows as two 16-row
         // slabs through a private one-slab buffer (its eighth of the staging
@@ -848,11 +875,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
           if (lane == 0) {
             // Counterfactual: the issuer is released only when its stores are complete.
             if (p.coupled) bulk_wait_all();
-            if (p.spans) {
-              const long long tile = static_cast<long long>(bh) * p.n_qtiles + qtile;
-              if (wq == 0) p.spans[2 * tile] = t0;
-              atomicMax(&p.spans[2 * tile + 1], static_cast<unsigned long long>(globaltimer_ns()));
-            }
+            if (p.spans) record_span_part(p, bh, qtile, t0, globaltimer_ns());
           }
         }
         tc_fence_before();
@@ -890,7 +913,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         ok = wait_phase(wg_sync, wgc & 1, abort_flag, lim);
         ++wgc;
         if (!__all_sync(0xffffffffu, ok)) goto teardown;
-        if (active && elected && !at_once) ss = StoreState{bh, qtile * BM, 0, 0, 0};
+        if (elected && !at_once) ss = StoreState{bh, qtile * BM, 0, 0, 0};
       }
     }
   }

@@ -122,7 +122,10 @@ def one_hot_case(B: int, N: int, H: int, d: int, seed: int, amplitude: float = 1
     perm = np.stack([np.stack([rng.permutation(N) for _ in range(H)]) for _ in range(B)])
     q = np.zeros((B, H, N, d), dtype=np.float32)
     q[..., :16] = amplitude * signs[perm]
-    bb, hh, jj, cc = np.meshgrid(np.arange(B), np.arange(H), j, np.arange(d), indexing="ij")
+    bb = np.arange(B, dtype=np.int64)[:, None, None, None]
+    hh = np.arange(H, dtype=np.int64)[None, :, None, None]
+    jj = j[None, None, :, None]
+    cc = np.arange(d, dtype=np.int64)[None, None, None, :]
     hashed = 1 + (jj * 2654435761 + cc * 40503 + hh * 9973 + bb * 7919 + int(seed)) % 250
     v = hashed.astype(np.float32)
     for c in range(4):

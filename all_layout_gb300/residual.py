@@ -12,18 +12,22 @@ For each sequence length N this measures, on one GPU and with the same kernel:
   T_fused     fused stores into the P destinations (xs_attn_fused, store_tile 8),
   T_coupled   the same with XS_FLAG_COMPLETION_COUPLED,
 and reports E_res / T_attn for both, a least-squares slope of E_res against N,
-and the distribution of per-tile store-issue spans (xs_attn_fused_ex spans).
+the distribution of per-tile store-issue spans (xs_attn_fused_ex spans), and
+the SM clocks and throttle reasons sampled while each N ran.
 
-Run as ``python -m all_layout_gb300.residual`` for a JSON report.
+Run as ``python -m all_layout_gb300.residual [--whole-units] [--markdown FILE]``.
 """
 from __future__ import annotations
 
 import json
+import sys
+import time
 
 import numpy as np
 import torch
 
-from . import xs
+from . import clocks, xs
+from .build import kernel_sha
 
 
 def _time_ms(fns, reps: int, flush: torch.Tensor) -> list:
@@ -74,10 +78,25 @@ def measure(N: int, H: int = 24, d: int = 128, P: int = 8, B: int = 1, reps: int
             "res_coupled": (t_coupled - t_attn) / t_attn, "spans": spans}
 
 
-def sweep(Ns=(1024, 2048, 4096, 8192, 16384, 32768, 65536), **kw) -> dict:
-    rows = [measure(N, reps=5 if N >= 32768 else 10, **kw) for N in Ns]
+def sweep(Ns=(1024, 2048, 4096, 8192, 16384, 32768, 65536), balanced: bool = True, **kw) -> dict:
+    ws = None
+    if balanced:
+        need = max(xs.workspace_bytes(1, N, kw.get("H", 24), kw.get("d", 128))[0] for N in Ns)
+        if need:
+            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            xs.set_workspace(ws)
+    rows = []
+    with clocks.ClockSampler(clocks.physical_gpu_index(torch.cuda.current_device())) as clk:
+        for N in Ns:
+            t0 = time.time()
+            r = measure(N, reps=5 if N >= 32768 else 10, **kw)
+            r["clocks"] = clk.summary(t0, time.time())
+            r["stream_k"] = int(ws is not None and xs.workspace_bytes(1, N, r["H"], r["d"])[1])
+            rows.append(r)
+    if ws is not None:
+        xs.set_workspace(None)
     x = np.array([r["N"] for r in rows], dtype=np.float64)
-    out = {"rows": rows}
+    out = {"rows": rows, "balanced": balanced}
     for key in ("fused", "coupled"):
         e = np.array([(r[f"t_{key}_ms"] - r["t_attn_ms"]) for r in rows])   # E_res in ms
         slope, icpt = np.polyfit(x, e, 1)
@@ -85,5 +104,39 @@ def sweep(Ns=(1024, 2048, 4096, 8192, 16384, 32768, 65536), **kw) -> dict:
     return out
 
 
+def markdown(rep: dict, command: str) -> str:
+    rows = rep["rows"]
+    out = ["# Residual-slope test: fused stores vs attention alone (Figure 11 analog, one GB300)", "",
+           f"Command (repository root): `{command}` (H=24, d=128, P=8, B=1, store_tile 8; L2",
+           "flushed before every timed call; median of 10 calls, 5 at N >= 32K, the three calls",
+           "interleaved round by round; " + ("a workspace registered, so each N takes the schedule the "
+                                             "cost model picks" if rep["balanced"] else
+                                             "no workspace: whole units") + ").",
+           "`coupled` = `xs_attn_fused_ex` with XS_FLAG_COMPLETION_COUPLED (each issuing warp waits for",
+           "its stores to complete, the pages' counterfactual). Span = per-tile store-issue span (first",
+           "slab issued -> last issuing warp released). SM clock: median of the nvidia-smi samples",
+           f"taken while that N ran. kernel_sha: {kernel_sha()}", "",
+           "| N | stream-K | T_attn ms | T_fused ms | T_coupled ms | E_res/T_attn fused | "
+           "E_res/T_attn coupled | span p50 / p99 (fused) | SM MHz | throttle reasons |",
+           "|---|---|---|---|---|---|---|---|---|---|"]
+    for r in rows:
+        c, s = r["clocks"], r["spans"]["fused"]
+        out.append(f"| {r['N']} | {'yes' if r['stream_k'] else 'no'} | {r['t_attn_ms']:.3f} | "
+                   f"{r['t_fused_ms']:.3f} | {r['t_coupled_ms']:.3f} | {100 * r['res_fused']:.2f}% | "
+                   f"{100 * r['res_coupled']:.2f}% | {s['p50_ns']:.0f} / {s['p99_ns']:.0f} ns | "
+                   f"{c['sm_mhz'] or '-'} | {', '.join(c['reasons']) or 'none'} |")
+    out += ["", f"Least-squares slope of E_res against N: fused "
+            f"{rep['slope_fused_us_per_1k_tokens']:.2f} us per 1K tokens, coupled "
+            f"{rep['slope_coupled_us_per_1k_tokens']:.2f} us per 1K tokens."]
+    return "\n".join(out) + "\n"
+
+
 if __name__ == "__main__":
-    print(json.dumps(sweep(), indent=1))
+    args = sys.argv[1:]
+    balanced = "--whole-units" not in args
+    rep = sweep(balanced=balanced)
+    if "--markdown" in args:
+        with open(args[args.index("--markdown") + 1], "w") as f:
+            f.write(markdown(rep, "python -m all_layout_gb300.residual"
+                             + ("" if balanced else " --whole-units")))
+    print(json.dumps(rep, indent=1))

@@ -7,6 +7,9 @@ plus fused vs serial (attention then the layout kernel) and attention-alone
 times on the same GPU.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl xs|reference]
+                       [--workload video_dit|peaked_16k|image_dit|small]
+The default workload is the largest single-GPU configuration, video-DiT
+B=1 N=65536 H=24 d=128 P=8.
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 (the (batch, head) problems are independent; no collective on the data path);
 value = total flops of all ranks / the slowest rank's time.
@@ -14,13 +17,10 @@ value = total flops of all ranks / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
 import re
-import subprocess
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -29,21 +29,26 @@ sys.path.insert(0, ROOT)
 METRIC = "fused attn+A2A-layout TFLOP/s & % bf16 peak; fused vs serial time (1 GB300)"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# ncu summaries of the fused kernel per workload (store_tile 8, balanced schedule).
-PROFILE_FILES = {"image_dit": os.path.join(ROOT, "profiles", "ncu_attn_fused_image_dit.md"),
-                 "peaked_16k": os.path.join(ROOT, "profiles", "ncu_attn_fused_peaked_16k.md")}
-KERNEL_SOURCES = ("all_layout_gb300/csrc/attn.cu", "all_layout_gb300/csrc/ptx.cuh",
-                  "all_layout_gb300/csrc/internal.h", "all_layout_gb300/csrc/api.cu")
+# ncu summaries of the fused kernel (store_tile 8, balanced schedule): workload ->
+# (summary file, the workload it captured). A workload without a capture of its own
+# takes the DRAM bytes of a capture of the same kernel on a smaller workload of the
+# same (H, d, P), scaled by the tokens processed: every launch reads q, k, v once
+# from HBM (the K/V of the heads in flight stay in L2) and writes the output once,
+# so its traffic grows in proportion to B*N*H*d.
+PROFILE_FILES = {"image_dit": ("ncu_attn_fused_image_dit.md", "image_dit"),
+                 "peaked_16k": ("ncu_attn_fused_peaked_16k.md", "peaked_16k"),
+                 "video_dit": ("ncu_attn_fused_peaked_16k.md", "peaked_16k")}
 L2_FLUSH_BYTES = 512 << 20
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("xs", "reference"), default="xs")
-    ap.add_argument("--workload", default="image_dit")
+    ap.add_argument("--workload", default="video_dit",
+                    help="one of all_layout_gb300.inputs.WORKLOADS (default: video-DiT N=65536)")
     ap.add_argument("--store-tile", type=int, default=None)
     ap.add_argument("--side-steps", type=int, default=100,
                     help="steps for the attention-alone / serial / scatter side timings")
@@ -63,91 +68,35 @@ def peaks():
 
 
 def kernel_sha() -> str:
-    h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
+    from all_layout_gb300.build import kernel_sha as _sha
+    return _sha()
 
 
 def profiled_traffic(workload: str, store_tile: int, balanced: bool):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary of
-    this workload, only if it was taken on the current kernel source and in the
-    launch configuration being timed (store_tile 8, balanced schedule)."""
-    path = PROFILE_FILES.get(workload)
-    if path is None or store_tile != 8 or not balanced:
-        return None
+    """(DRAM bytes per launch, how it was obtained) of the fused kernel from the
+    committed ncu summary for this workload, only if that summary was taken on the
+    current kernel source and in the launch configuration being timed (store_tile
+    8, balanced schedule); (None, reason) otherwise."""
+    from all_layout_gb300 import inputs
+    entry = PROFILE_FILES.get(workload)
+    if entry is None:
+        return None, "no ncu capture for this workload"
+    if store_tile != 8 or not balanced:
+        return None, "ncu captures cover store_tile 8 with the balanced schedule only"
+    fname, captured = entry
     try:
-        text = open(path).read()
+        text = open(os.path.join(ROOT, "profiles", fname)).read()
     except OSError:
-        return None
+        return None, f"profiles/{fname} missing"
     sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", text)
     tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not sha or not tb or sha.group(1) != kernel_sha():
-        return None
-    return float(tb.group(1))
-
-
-class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
-        self.thread = None
-
-    def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-            time.sleep(0.3)
-        except OSError:
-            self.proc = None
-        return self
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
-
-    def __exit__(self, *exc):
-        if self.proc:
-            time.sleep(0.15)
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-
-    def summary(self, t0: float, t1: float):
-        sm, mx, reasons = [], None, set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ts, line in self.lines:
-            if ts < t0 or ts > t1:
-                continue
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return None, f"profiles/{fname} was taken on another kernel source"
+    w, c = inputs.WORKLOADS[workload], inputs.WORKLOADS[captured]
+    scale = (w.B * w.N * w.H * w.d) / (c.B * c.N * c.H * c.d)
+    how = f"ncu profiles/{fname}" + ("" if scale == 1 else
+                                     f" ({c.name}), scaled x{scale:g} by tokens processed")
+    return float(tb.group(1)) * scale, how
 
 
 def dist_setup(n_gpus):
@@ -241,7 +190,7 @@ def run_reference(args, w, rank, world):
 def run_xs(args, w, rank, world, local):
     import torch
 
-    from all_layout_gb300 import inputs, xs
+    from all_layout_gb300 import clocks, inputs, xs
 
     st = args.store_tile or w.store_tile
     dev = torch.device("cuda", local)
@@ -278,14 +227,8 @@ def run_xs(args, w, rank, world, local):
         fused()
     torch.cuda.synchronize(dev)
 
-    gpu_index = local
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-    if vis:
-        try:
-            gpu_index = int(vis.split(",")[local])
-        except ValueError:
-            pass
-    with ClockSampler(gpu_index) as clk:
+    gpu_index = clocks.physical_gpu_index(local)
+    with clocks.ClockSampler(gpu_index) as clk:
         barrier(world)
         torch.cuda.synchronize(dev)
         t0 = time.time()
@@ -299,7 +242,7 @@ def run_xs(args, w, rank, world, local):
     ms_per_step = total_ms / args.steps
     flops = w.flops
     value = flops * world / (ms_per_step * 1e-3) / 1e12
-    clocks = clk.summary(t0, t1)
+    clock_rec = clk.summary(t0, t1)
 
     # Side timings on the same GPU: attention alone, serial path, layout kernel alone.
     side = max(5, args.side_steps)
@@ -376,18 +319,21 @@ def run_xs(args, w, rank, world, local):
     pk, pk_kind = peaks()
     peak = float(pk["bf16_tflops"])
     achieved = flops / (ms_per_step * 1e-3) / 1e12        # per launch, this rank's GPU
+    traffic, traffic_how = profiled_traffic(args.workload, st, workspace is not None)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_kind": f"{pk_kind} bf16 (burst)",
-                "traffic": profiled_traffic(args.workload, st, workspace is not None),
+                "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
+                "traffic": traffic, "traffic_source": traffic_how,
+                "algorithmic_bytes": 4 * w.B * w.H * w.N * w.d * 2,
                 "kernel": "attn_kernel<%d> (fused)" % w.d,
                 "kernel_sha": kernel_sha()}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows = w.N if w.N <= 8192 else 256     # whole workload when it takes seconds
+        rows = w.N if w.N <= 8192 else 512     # whole workload when it takes seconds
         val, dt, thr, desc = cpu_oracle_sample(w, rows)
         cpu = {"value": val, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+               "seconds": dt, "extrapolated_full_s": dt * w.N / rows}
 
     if rank == 0:
         line = {
@@ -407,7 +353,7 @@ def run_xs(args, w, rank, world, local):
             "fused_over_attn": t_fused_med / med(t_attn),
             "serial_over_fused": med(t_serial) / t_fused_med,
             "hiding_ratio": (med(t_serial) - t_fused_med) / med(t_scatter),
-            "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": clock_rec, "e2e": e2e,
             "gpu_launches": args.steps,
         }
         print(json.dumps(line), flush=True)

@@ -187,10 +187,12 @@ xs_status xs_store_burst_probe(void *dst, unsigned long long dst_bytes, int K,
  * loads the library holds until the process exits. Nothing is allocated:
  * no cudaMalloc, cudaFree or allocating library call.
  *   - XS_ERR_INVALID if B*H*N*d*2 bytes exceed XS_NOALLOC_SCRATCH_BYTES
- *     (checked first, before any device work).
- *   - The first call on each device (with that device current) looks up the
- *     array's device address and caches it; make that first call before any
- *     stream capture.
+ *     (checked first, factor by factor so no product wraps, before any device
+ *     work).
+ *   - Every call looks up the array's device address on the current device
+ *     (a symbol lookup, no allocation), so a device reset that reloads the
+ *     library's device code cannot leave a stale address in use. The first
+ *     call on a device may load that code: make it before any stream capture.
  *   - Every call on a device shares the one array and leaves the last call's o
  *     in it (each call overwrites all of the o it reads, so nothing needs
  *     clearing). Calls that overlap on the GPU (different streams, or

@@ -55,3 +55,20 @@ def gather_rows(got_shards: np.ndarray, rows: np.ndarray, N: int, P: int) -> np.
     p, i = rows // R, rows % R
     sel = got_shards[p, :, i]              # [len(rows), B, H, d]
     return np.transpose(sel, (1, 2, 0, 3))
+
+
+def gather_rows_dev(shards, rows: np.ndarray, N: int, P: int) -> np.ndarray:
+    """Pick query rows from P device shards [B, N/P, H, d] on the GPU and return
+    them as float64 [B, H, len(rows), d] (only the sampled rows leave the device)."""
+    R = N // P
+    out = []
+    for r in rows:
+        p, i = int(r) // R, int(r) % R
+        out.append(shards[p][:, i])                        # [B, H, d]
+    sel = torch.stack(out, dim=2)                         # [B, H, rows, d]
+    return sel.float().cpu().numpy().astype(np.float64)
+
+
+def all_finite_dev(shards) -> bool:
+    """Every element of every device shard is finite (no NaN fill left)."""
+    return all(bool(torch.isfinite(s).all()) for s in shards)

@@ -241,6 +241,27 @@ def test_ulysses_one_hot_exact_and_untouched_heads(xs):
 
 # ------------------------------------------------------------------ experiment controls
 
+@pytest.mark.parametrize("B,H,N,d,P,st,flags", [(1, 3, 1024, 128, 4, 8, 1), (2, 2, 640, 64, 5, 8, 1),
+                                                 (1, 3, 1024, 128, 4, 2, 0), (1, 2, 384, 64, 3, 8, 0)])
+def test_fused_ex_vs_oracle(xs, B, H, N, d, P, st, flags):
+    """xs_attn_fused_ex against the oracle itself (not only against xs_attn_fused):
+    the completion-coupled counterfactual and span recording change when stores
+    are waited for, never what is stored."""
+    q, k, v = inputs.qkv(B, N, H, d, seed=63 + N)
+    out = xs.alloc_shards(B, N, H, d, P)
+    for s in out:
+        s.fill_(float("nan"))
+    n_tiles = B * H * (N // 128)
+    spans = torch.zeros(2 * n_tiles, dtype=torch.int64, device="cuda")
+    xs.attn_fused_ex(*_dev(q, k, v), out, store_tile=st, flags=flags, spans=spans)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    assert_close(shards_f64(out), oracle.shard_layout(oracle.attention(q, k, v), P),
+                 f"fused_ex st={st} flags={flags}")
+    t = spans.view(n_tiles, 2).cpu().numpy()
+    assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])
+
+
 @pytest.mark.parametrize("st,flags", [(8, 0), (8, 1), (2, 0)])
 def test_fused_ex_spans_and_coupled_bytes(xs, st, flags):
     B, H, N, d, P = 1, 3, 1024, 128, 4
@@ -302,3 +323,39 @@ def test_unaligned_to_128_bytes_but_16(xs):
     torch.cuda.synchronize()
     assert xs.last_device_status() == xs.OK
     assert_close(shards_f64(shards), oracle.shard_layout(oracle.attention(q, k, v), P), "offset buffers")
+
+
+# ------------------------------------------------------------------ tensor-map cache
+
+def test_same_addresses_new_shapes_and_many_buffers(xs):
+    """The library keeps encoded tensor maps keyed by address and shape: buffers
+    reused at the same addresses for a different shape, and more distinct buffers
+    than the cache holds, must still give oracle results."""
+    big = [torch.empty(1 << 21, dtype=torch.bfloat16, device="cuda") for _ in range(3 + 8)]
+    for (B, H, N, d, P) in [(1, 2, 512, 128, 4), (1, 4, 256, 64, 2), (2, 1, 384, 128, 3)]:
+        q, k, v = inputs.qkv(B, N, H, d, seed=3 * N + H)
+        n = B * H * N * d
+        qd, kd, vd = (buf[:n].view(B, H, N, d) for buf in big[:3])
+        for src, dst in ((q, qd), (k, kd), (v, vd)):
+            dst.copy_(src.cuda())
+        shards = [buf[:n // P].view(B, N // P, H, d) for buf in big[3:3 + P]]
+        for s in shards:
+            s.fill_(float("nan"))
+        xs.attn_fused(qd, kd, vd, shards, store_tile=8)
+        torch.cuda.synchronize()
+        assert xs.last_device_status() == xs.OK
+        assert_close(shards_f64(shards), oracle.shard_layout(oracle.attention(q, k, v), P),
+                     f"reused addresses B{B} H{H} N{N} d{d} P{P}")
+    # 40 calls on distinct buffers: 440 maps, beyond what the cache keeps
+    B, H, N, d, P = 1, 1, 128, 64, 8
+    q, k, v = inputs.qkv(B, N, H, d, seed=5)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    keep = []
+    for i in range(40):
+        qd, kd, vd = _dev(q, k, v)
+        shards = xs.alloc_shards(B, N, H, d, P)
+        xs.attn_fused(qd, kd, vd, shards, store_tile=8)
+        keep.append((qd, kd, vd, shards))
+    torch.cuda.synchronize()
+    for (_, _, _, shards) in keep[::13]:
+        assert_close(shards_f64(shards), ref, "many buffers")

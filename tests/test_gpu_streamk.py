@@ -15,7 +15,8 @@ import torch
 
 import oracle
 from all_layout_gb300 import inputs
-from gpu_util import assert_close, gather_rows, sample_rows, shards_bits, shards_f64
+from gpu_util import (all_finite_dev, assert_close, gather_rows, gather_rows_dev, sample_rows,
+                      shards_bits, shards_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -198,3 +199,76 @@ def test_streamk_ulysses_both_all_to_alls(xs, ws):
     assert xs.last_device_status() == xs.OK
     ref = oracle.shard_layout(oracle.attention(q, k, v), P)
     assert_close(shards_f64(out), ref, "ulysses stream-K")
+
+
+# ------------------------------------------------------------------ the benchmark's launch
+
+def test_streamk_video_dit_sampled(xs):
+    """The video-DiT workload (B1 N65536 H24 d128 P8) in the launch configuration the
+    benchmark times: the workspace it registers (xs.alloc_workspace), store_tile 8.
+    Sampled rows (every destination's first and last row, every slab position,
+    random rows) against the oracle, and every destination element written."""
+    w = inputs.WORKLOADS["video_dit"]
+    assert _cut(xs, w.B, w.N, w.H, w.d) == 1, "the benchmark's launch takes the balanced schedule"
+    q, k, v = inputs.workload_qkv(w)
+    ws = xs.alloc_workspace(w.B, w.N, w.H, w.d)
+    try:
+        shards = _fused(xs, q, k, v, w.P, w.store_tile)
+    finally:
+        xs.set_workspace(None)
+    del ws
+    assert all_finite_dev(shards)
+    rows = sample_rows(w.N, w.P, np.random.default_rng(w.seed), extra=16)
+    assert_close(gather_rows_dev(shards, rows, w.N, w.P), oracle.attention_rows(q, k, v, rows),
+                 w.name + " stream-K")
+
+
+@pytest.mark.parametrize("st", [8, 2])
+def test_streamk_one_hot_exact_64k(xs, ws, st):
+    """Exact placement at N = 65536 under the balanced schedule: the matching key
+    out-scores the 16 keys one bit away by 2*128/sqrt(128) (the rest by more), so the
+    other weights sum to < 2^-28 and every output row is V's row perm[n] bit for bit,
+    whichever CTA finishes its pieces."""
+    B, H, N, d, P = 1, 2, 65536, 128, 8
+    assert _cut(xs, B, N, H, d) == 1
+    q, k, v, perm = inputs.one_hot_case(B, N, H, d, seed=23)
+    got = shards_bits(_fused(xs, q, k, v, P, st))
+    o_exp = np.take_along_axis(inputs.bits(v), perm[..., None].repeat(d, axis=3), axis=2)
+    exp = oracle.shard_layout(o_exp, P)
+    if not np.array_equal(got, exp):
+        bad = np.argwhere(got != exp)
+        raise AssertionError(f"{len(bad)} mismatching elements, first at {tuple(bad[0])}")
+
+
+@pytest.mark.parametrize("idx", [5, 30, 55, 89])
+def test_sweep_points_sampled_with_workspace(xs, ws, idx):
+    """The sweep points of the whole-unit parity test, in the schedule the sweep
+    times (a workspace registered)."""
+    w = inputs.sweep_points()[idx]
+    q, k, v = inputs.workload_qkv(w)
+    shards = _fused(xs, q, k, v, w.P, w.store_tile)
+    assert all_finite_dev(shards)
+    rows = sample_rows(w.N, w.P, np.random.default_rng(w.seed), extra=8)
+    assert_close(gather_rows_dev(shards, rows, w.N, w.P), oracle.attention_rows(q, k, v, rows),
+                 w.name + (" stream-K" if _cut(xs, w.B, w.N, w.H, w.d) else " whole units"))
+
+
+@pytest.mark.parametrize("st,flags", [(8, 0), (8, 1), (2, 0)])
+def test_streamk_fused_ex_vs_oracle(xs, ws, st, flags):
+    """xs_attn_fused_ex (completion-coupled flag, per-tile spans) against the oracle
+    under the balanced schedule."""
+    B, H, N, d, P = 1, 2, 2944, 128, 4
+    assert _cut(xs, B, N, H, d) == 1
+    q, k, v = inputs.qkv(B, N, H, d, seed=67)
+    out = xs.alloc_shards(B, N, H, d, P)
+    for s in out:
+        s.fill_(float("nan"))
+    n_tiles = B * H * (N // 128)
+    spans = torch.zeros(2 * n_tiles, dtype=torch.int64, device="cuda")
+    xs.attn_fused_ex(*_dev(q, k, v), out, store_tile=st, flags=flags, spans=spans)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    assert_close(shards_f64(out), oracle.shard_layout(oracle.attention(q, k, v), P),
+                 f"fused_ex st={st} flags={flags}")
+    t = spans.view(n_tiles, 2).cpu().numpy()
+    assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])

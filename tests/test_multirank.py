@@ -58,17 +58,27 @@ def test_reference_arm_two_ranks_prints_once():
 
 
 def test_roofline_traffic_only_for_the_profiled_launch():
-    """The bench reports a DRAM traffic figure only for a workload with a committed
-    ncu summary, taken on the current kernel source, in the launch configuration
-    being timed (store_tile 8, balanced schedule); otherwise null."""
+    """The bench reports a DRAM traffic figure only from a committed ncu summary
+    taken on the current kernel source, in the launch configuration being timed
+    (store_tile 8, balanced schedule); a workload without a capture of its own
+    takes a capture of the same (H, d, P) scaled by the tokens processed;
+    otherwise null with the reason."""
+    import os
     import re
     import bench
-    for key, path in bench.PROFILE_FILES.items():
-        text = open(path).read()
+    from all_layout_gb300 import inputs
+    for key, (fname, captured) in bench.PROFILE_FILES.items():
+        text = open(os.path.join(ROOT, "profiles", fname)).read()
         sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", text).group(1)
         tb = float(re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text).group(1))
-        want = tb if sha == bench.kernel_sha() else None
-        assert bench.profiled_traffic(key, 8, True) == want
-        assert bench.profiled_traffic(key, 4, True) is None
-        assert bench.profiled_traffic(key, 8, False) is None
-    assert bench.profiled_traffic("video_dit", 8, True) is None
+        w, c = inputs.WORKLOADS[key], inputs.WORKLOADS[captured]
+        assert (w.H, w.d, w.P, w.B) == (c.H, c.d, c.P, c.B)
+        scale = w.N / c.N
+        got, how = bench.profiled_traffic(key, 8, True)
+        if sha == bench.kernel_sha():
+            assert got == tb * scale and fname in how
+        else:
+            assert got is None and "another kernel source" in how
+        assert bench.profiled_traffic(key, 4, True)[0] is None
+        assert bench.profiled_traffic(key, 8, False)[0] is None
+    assert bench.profiled_traffic("small", 8, True)[0] is None
