@@ -463,6 +463,16 @@ XS_API xs_status xs_selftest_bounded_wait(void *stream) {
              : XS_ERR_CUDA;
 }
 
+XS_API xs_status xs_selftest_exp2(const float *x, float *out_poly, float *out_mufu, int n,
+                                  void *stream) {
+  if (!x || !out_poly || !out_mufu || n < 0) return XS_ERR_INVALID;
+  if (n == 0) return XS_OK;
+  return xs::launch_exp2_selftest(x, out_poly, out_mufu, n, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? XS_OK
+             : XS_ERR_CUDA;
+}
+
 XS_API xs_status xs_set_workspace(void *ws, unsigned long long bytes, void *stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XS_ERR_CUDA;

@@ -51,6 +51,13 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#ifndef XS_POLY_PAIRS_D64
+#define XS_POLY_PAIRS_D64 2
+#endif
+#ifndef XS_POLY_PAIRS_D128
+#define XS_POLY_PAIRS_D128 0
+#endif
+
 namespace xs {
 
 __device__ int g_status;
@@ -66,6 +73,19 @@ constexpr int kLoadWarp = 9;
 constexpr int kHalfBytes = BM * 128;     // one 64-column half of a 128-row tile
 constexpr uint32_t kWaitSleepNs = 100000;   // longest suspension per try in a blocked wait
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+// Exponentials per 32 of a row computed by the polynomial (exp2_poly_x2) instead
+// of MUFU ex2, as pairs: the pairs i of a 32-column chunk with i % 16 in the
+// template's set. At d = 64 the two tiles' softmax phases overlap on each SMSP
+// and the MUFU unit is the bound; moving a share to the FMA pipe balances them.
+template <int D>
+struct PolyPairs {
+  static constexpr int N = (D == 64) ? XS_POLY_PAIRS_D64 : XS_POLY_PAIRS_D128;
+  // pair i (0..15) of each chunk goes to the polynomial: spread evenly
+  static __device__ __forceinline__ constexpr bool take(int i) {
+    return N > 0 && (i * N) % 16 < N;
+  }
+};
 
 template <int D, bool SHARED>
 struct Cfg {
@@ -809,9 +829,15 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         for (int i = 0; i < 16; ++i) {
           const uint64_t x2 = f2_fma(
               f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])), scale2, negm2);
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          float p0, p1;
+          if (PolyPairs<D>::take(i)) {
+            f2_unpack(exp2_poly_x2(x2), p0, p1);
+          } else {
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
           lsum[i & 3] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
@@ -997,7 +1023,29 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
   __syncthreads();
 }
 
+// Element i: out_poly[i] = the kernel's polynomial 2^x[i], out_mufu[i] = ex2.approx.ftz(x[i]).
+__global__ void exp2_selftest_kernel(const float *x, float *out_poly, float *out_mufu, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float a = x[i], b = i + 1 < n ? x[i + 1] : 0.f;
+  float p0, p1;
+  f2_unpack(exp2_poly_x2(f2_pack(a, b)), p0, p1);
+  out_poly[i] = p0;
+  out_mufu[i] = ex2_approx(a);
+  if (i + 1 < n) {
+    out_poly[i + 1] = p1;
+    out_mufu[i + 1] = ex2_approx(b);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_exp2_selftest(const float *x, float *out_poly, float *out_mufu, int n,
+                                 cudaStream_t s) {
+  const int pairs = (n + 1) / 2;
+  exp2_selftest_kernel<<<(pairs + 255) / 256, 256, 0, s>>>(x, out_poly, out_mufu, n);
+  return cudaGetLastError();
+}
 
 int attn_smem_bytes(int d) {
   return d == 128 ? Cfg<128, false>::SMEM : Cfg<64, false>::SMEM;

@@ -63,6 +63,8 @@ cudaError_t launch_burst_probe(void *dst, int K, long long burst_bytes, int n_bu
                                long long gap_ns, int mode, unsigned long long *times,
                                cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
+cudaError_t launch_exp2_selftest(const float *x, float *out_poly, float *out_mufu, int n,
+                                 cudaStream_t s);
 cudaError_t read_and_clear_status(cudaStream_t s, int *out);
 
 }  // namespace xs

@@ -274,6 +274,43 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t f2_add_rm(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rm.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^x for a pair of fp32 values on the FMA and ALU pipes, leaving the MUFU unit
+// to the other exponentials of the row. Range reduction in the manner of Cody
+// and Waite: n = floor(x) (adding 1.5 * 2^23 with round-down leaves n in the low
+// mantissa bits), f = x - n in [0, 1) exactly; 2^f from a degree-3 polynomial
+// with minimax relative error 7.5e-5 on [0, 1] (Remez exchange; the
+// coefficients are written by exp2_poly_fit.py beside this file); 2^n added to
+// the exponent field. Arguments below -126 are raised to -126 (the result, at
+// most 2^-126, then stays a tiny positive number instead of wrapping the
+// exponent); arguments are at most a few units above 0 here.
+__device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x2) {
+  constexpr float c0 = 0.9999251961708069f, c1 = 0.6958335638046265f;
+  constexpr float c2 = 0.22606715559959412f, c3 = 0.07802452147006989f;
+  float x0, x1;
+  f2_unpack(x2, x0, x1);
+  const uint64_t x = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+  const uint64_t magic = f2_pack(12582912.f, 12582912.f);
+  const uint64_t t = f2_add_rm(x, magic);
+  const uint64_t f = f2_sub(x, f2_sub(t, magic));
+  uint64_t p = f2_fma(f, f2_pack(c3, c3), f2_pack(c2, c2));
+  p = f2_fma(p, f, f2_pack(c1, c1));
+  p = f2_fma(p, f, f2_pack(c0, c0));
+  const uint32_t t_lo = static_cast<uint32_t>(t), t_hi = static_cast<uint32_t>(t >> 32);
+  const uint32_t p_lo = static_cast<uint32_t>(p), p_hi = static_cast<uint32_t>(p >> 32);
+  return (static_cast<uint64_t>(p_hi + (t_hi << 23)) << 32) | (p_lo + (t_lo << 23));
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -54,6 +54,8 @@ _lib.xs_selftest_bounded_wait.argtypes = [_vp]
 _lib.xs_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
 _lib.xs_set_wait_limit_ns.restype = ctypes.c_ulonglong
 _lib.xs_abi_version.restype = _i
+_lib.xs_selftest_exp2.argtypes = [_vp, _vp, _vp, _i, _vp]
+_lib.xs_selftest_exp2.restype = _i
 _lib.xs_set_workspace.argtypes = [_vp, ctypes.c_ulonglong, _vp]
 _lib.xs_set_workspace.restype = _i
 _lib.xs_workspace_bytes.argtypes = [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong),
@@ -197,6 +199,15 @@ def set_wait_limit_ns(limit_ns: int) -> int:
 
 def selftest_bounded_wait(stream=None):
     _check(_lib.xs_selftest_bounded_wait(_stream(stream)), "xs_selftest_bounded_wait")
+
+
+def selftest_exp2(x, stream=None):
+    """(polynomial 2^x, MUFU 2^x) for a float32 CUDA tensor x (see xs_selftest_exp2)."""
+    x = x.contiguous()
+    poly, mufu = torch.empty_like(x), torch.empty_like(x)
+    _check(_lib.xs_selftest_exp2(_ptr(x), _ptr(poly), _ptr(mufu), x.numel(), _stream(stream)),
+           "xs_selftest_exp2")
+    return poly, mufu
 
 
 def alloc_shards(B, N, H, d, P, device="cuda"):

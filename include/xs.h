@@ -263,6 +263,15 @@ unsigned long long xs_set_wait_limit_ns(unsigned long long limit_ns);
  * outcome with xs_last_device_status. */
 xs_status xs_selftest_bounded_wait(void *stream);
 
+/* Self-test of the softmax's two exponential paths: for i < n (device fp32
+ * buffers), out_poly[i] = 2^x[i] as the attention kernel's polynomial computes
+ * it on the FMA pipe for a share of each row (range reduction x = n + f,
+ * degree-3 minimax polynomial for 2^f, n added to the exponent; arguments below
+ * -126 raised to -126), out_mufu[i] = 2^x[i] from the MUFU unit (ex2.approx,
+ * subnormal results flushed to zero). For tests comparing the two against each
+ * other and against an error bound. XS_ERR_INVALID for NULL pointers or n < 0. */
+xs_status xs_selftest_exp2(const float *x, float *out_poly, float *out_mufu, int n, void *stream);
+
 /* ABI version of this header (1). */
 int xs_abi_version(void);
 
