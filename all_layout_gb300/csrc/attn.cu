@@ -51,12 +51,6 @@
 #include "internal.h"
 #include "ptx.cuh"
 
-#ifndef XS_POLY_PAIRS_D64
-#define XS_POLY_PAIRS_D64 2
-#endif
-#ifndef XS_POLY_PAIRS_D128
-#define XS_POLY_PAIRS_D128 0
-#endif
 
 namespace xs {
 
@@ -74,17 +68,17 @@ constexpr int kHalfBytes = BM * 128;     // one 64-column half of a 128-row tile
 constexpr uint32_t kWaitSleepNs = 100000;   // longest suspension per try in a blocked wait
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
-// Exponentials per 32 of a row computed by the polynomial (exp2_poly_x2) instead
-// of MUFU ex2, as pairs: the pairs i of a 32-column chunk with i % 16 in the
-// template's set. At d = 64 the two tiles' softmax phases overlap on each SMSP
-// and the MUFU unit is the bound; moving a share to the FMA pipe balances them.
+// Exponentials computed by the polynomial (exp2_poly_x2) instead of MUFU ex2:
+// the pairs i of each 32-column chunk with (i * N) % 16 < N, i.e. N of every 16
+// pairs spread evenly. Measured at N = 16384 (TFLOP/s for N = 0, 1, 2, 3, 4, 6):
+// d = 64 H = 48: 1105, 1105, 1085, 1003, 865, 861; d = 128 H = 24: 1764, 1779,
+// 1632 for N = 0, 1, 2. The softmax is not bound by the MUFU unit here (its
+// exponential phase is issue- and latency-bound, and the polynomial costs ten
+// instructions per pair against two MUFU issues), so no pair takes it.
 template <int D>
 struct PolyPairs {
-  static constexpr int N = (D == 64) ? XS_POLY_PAIRS_D64 : XS_POLY_PAIRS_D128;
-  // pair i (0..15) of each chunk goes to the polynomial: spread evenly
-  static __device__ __forceinline__ constexpr bool take(int i) {
-    return N > 0 && (i * N) % 16 < N;
-  }
+  static constexpr int N = 0;
+  static __device__ __forceinline__ constexpr bool take(int i) { return N > 0 && (i * N) % 16 < N; }
 };
 
 template <int D, bool SHARED>
