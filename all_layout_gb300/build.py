@@ -19,6 +19,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libxs.so")
 SOURCES = ("attn.cu", "scatter.cu", "api.cu", "noalloc.cu", "probe.cu")
 HEADERS = (os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"),
+           os.path.join(CSRC, "attn_wide.cuh"),
            os.path.join(ROOT, "include", "xs.h"))
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden"]
@@ -26,7 +27,7 @@ NVCC_FLAGS = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvis
 
 # Sources of the attention kernel and its launch path: their hash names the kernel
 # build that a measurement or an ncu summary was taken on.
-KERNEL_SOURCES = ("attn.cu", "ptx.cuh", "internal.h", "api.cu")
+KERNEL_SOURCES = ("attn.cu", "ptx.cuh", "internal.h", "api.cu", "attn_wide.cuh")
 
 
 def kernel_sha() -> str:

@@ -135,7 +135,9 @@ xs_status validate(const void *const *ptrs, int nptrs, void *const *shards, int 
   }
   if (store_tile != 1 && store_tile != 2 && store_tile != 4 && store_tile != 8)
     return XS_ERR_INVALID;
-  if (d != 64 && d != 128) return XS_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return XS_ERR_UNSUPPORTED;
+  // d = 256 stores each finished tile at once (no room to stage a deferred one).
+  if (d == 256 && store_tile != 8) return XS_ERR_UNSUPPORTED;
   if (N % xs::kTileRows != 0) return XS_ERR_UNSUPPORTED;
   for (int i = 0; i < nptrs; ++i)
     if (!aligned16(ptrs[i])) return XS_ERR_ALIGN;
@@ -289,9 +291,10 @@ xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B
   prm.coupled = coupled;
   prm.spans = spans;
   prm.shared_staging = store_tile == 8 ? 1 : 0;
-  prm.kv_stages = xs::attn_kv_stages(d, store_tile == 8);
+  prm.kv_stages = d == 256 ? 0 : xs::attn_kv_stages(d, store_tile == 8);
   prm.n_qtiles = N / xs::kTileRows;
-  prm.n_pairs = (prm.n_qtiles + 1) / 2;
+  // d <= 128: a unit is a pair of query tiles; d = 256: a single tile.
+  prm.n_pairs = d == 256 ? prm.n_qtiles : (prm.n_qtiles + 1) / 2;
   prm.n_units = B * H * prm.n_pairs;
   prm.n_kv = N / xs::kTileRows;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
@@ -437,7 +440,9 @@ XS_API const char *xs_status_string(xs_status s) {
   switch (s) {
     case XS_OK: return "ok";
     case XS_ERR_INVALID: return "invalid argument";
-    case XS_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, N a multiple of 128)";
+    case XS_ERR_UNSUPPORTED:
+      return "unsupported shape (d must be 64, 128 or 256, N a multiple of 128; d = 256 needs "
+             "store_tile 8)";
     case XS_ERR_ALIGN: return "pointer not 16-byte aligned";
     case XS_ERR_CUDA: return "CUDA error";
     case XS_ERR_TIMEOUT: return "on-chip wait timed out";
@@ -492,7 +497,7 @@ XS_API xs_status xs_set_workspace(void *ws, unsigned long long bytes, void *stre
 XS_API xs_status xs_workspace_bytes(int B, int N, int H, int d, unsigned long long *bytes,
                                     int *cut) {
   if (!bytes || B < 0 || N < 0 || H < 0) return XS_ERR_INVALID;
-  if (d != 64 && d != 128) return XS_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return XS_ERR_UNSUPPORTED;
   if (N % xs::kTileRows != 0) return XS_ERR_UNSUPPORTED;
   *bytes = 0;
   if (cut) *cut = 0;
@@ -500,7 +505,8 @@ XS_API xs_status xs_workspace_bytes(int B, int N, int H, int d, unsigned long lo
   const int sms = sm_count();
   if (sms <= 0) return XS_ERR_CUDA;
   const int n_qtiles = N / xs::kTileRows;
-  const int units = B * H * ((n_qtiles + 1) / 2);
+  // d <= 128: a unit is a pair of query tiles; d = 256: a single tile.
+  const int units = B * H * (d == 256 ? n_qtiles : (n_qtiles + 1) / 2);
   const Plan pl = plan_launch(units, sms, n_qtiles, d, ~0ull);
   *bytes = pl.bytes;
   if (cut) *cut = pl.sk;

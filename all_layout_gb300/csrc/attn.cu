@@ -1001,6 +1001,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   }
 }
 
+#include "attn_wide.cuh"
+
 __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -1042,6 +1044,7 @@ cudaError_t launch_exp2_selftest(const float *x, float *out_poly, float *out_muf
 }
 
 int attn_smem_bytes(int d) {
+  if (d == 256) return wide::SMEM;
   return d == 128 ? Cfg<128, false>::SMEM : Cfg<64, false>::SMEM;
 }
 
@@ -1061,6 +1064,13 @@ static cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_attn(const AttnParams &p, int d, int grid, cudaStream_t s) {
+  if (d == 256) {
+    cudaError_t e = cudaFuncSetAttribute(wide::attn_wide_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, wide::SMEM);
+    if (e != cudaSuccess) return e;
+    wide::attn_wide_kernel<<<grid, wide::kThreadsW, wide::SMEM, s>>>(p);
+    return cudaGetLastError();
+  }
   const bool shared = p.shared_staging != 0;
   if (d == 128) return shared ? launch_one<128, true>(p, grid, s) : launch_one<128, false>(p, grid, s);
   return shared ? launch_one<64, true>(p, grid, s) : launch_one<64, false>(p, grid, s);

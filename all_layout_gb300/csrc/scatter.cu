@@ -2,7 +2,7 @@
 // separate A2A step of serial execution; X-Stage abstract and Figure 5 (e)):
 //   o [B][H][N][d]  ->  shard p [B][N/P][H][d],  p = n / (N/P), i = n % (N/P).
 // HBM-bound: every byte is read once and written once. Each row of d bf16
-// (128 or 256 contiguous bytes on both sides) is moved by d/8 lanes with one
+// (128, 256 or 512 contiguous bytes on both sides) is moved by d/8 lanes with one
 // 16-byte vector each, so a warp touches whole 128-byte lines on both sides.
 #include <cstdint>
 
@@ -67,7 +67,10 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4 *__restrict__ 
 cudaError_t launch_scatter(const void *o, const ShardPtrs &sh, int B, int N, int H, int d,
                            int rows_per_shard, int grid, cudaStream_t s) {
   const long long rows = static_cast<long long>(B) * H * N;
-  if (d == 128)
+  if (d == 256)
+    scatter_kernel<256><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(o), sh, N, H,
+                                             rows_per_shard, rows);
+  else if (d == 128)
     scatter_kernel<128><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(o), sh, N, H,
                                              rows_per_shard, rows);
   else

@@ -44,7 +44,10 @@
  *      XS_ERR_INVALID     a NULL pointer (also any NULL shard), B, N or H < 0,
  *                         P not in [1, 8], N % P != 0,
  *                         store_tile not in {1, 2, 4, 8};
- *      XS_ERR_UNSUPPORTED d not in {64, 128}, or N % 128 != 0;
+ *      XS_ERR_UNSUPPORTED d not in {64, 128, 256}, N % 128 != 0, or d = 256
+ *                         with store_tile != 8 (at d = 256 every finished tile
+ *                         is stored at once: a deferred tile does not fit on
+ *                         chip beside the K/V ring);
  *      XS_ERR_ALIGN       a pointer that is not 16-byte aligned.
  *    B == 0, H == 0 or N == 0 is an empty problem: the call validates its
  *    other arguments and returns XS_OK without launching anything.
@@ -67,15 +70,16 @@ typedef enum {
 
 /* Fused attention + shard layout (abstract: tile-granular fusion of the
  * post-attention All-to-All with FlashAttention; Figure 7). One persistent
- * kernel. Each finished 128-row output tile is staged on chip and written into
- * the P shards by the warps that own it, in bursts of `store_tile` 16-row slabs
- * interleaved with the KV iterations of that warp group's next tile
- * (store_tile = 8, or a tile with no next tile on its SM: the whole tile
- * right after it is finished).
+ * kernel (d = 64 and 128: two query tiles per CTA; d = 256: one query tile per
+ * CTA with its scores double-buffered on chip). Each finished 128-row output
+ * tile is staged on chip and written into the P shards by the warps that own
+ * it, in bursts of `store_tile` 16-row slabs interleaved with the KV
+ * iterations of that warp group's next tile (store_tile = 8, or a tile with no
+ * next tile on its SM: the whole tile right after it is finished).
  * The result does not depend on store_tile.
  *   q, k, v     [B][H][N][d] bf16, device.
  *   out_shards  host array of P device pointers, shard p [B][N/P][H][d] bf16.
- *   store_tile  1, 2, 4 or 8 slabs per burst. */
+ *   store_tile  1, 2, 4 or 8 slabs per burst (8 only at d = 256). */
 xs_status xs_attn_fused(const void *q, const void *k, const void *v,
                         void *const *out_shards, int B, int N, int H, int d,
                         int P, int store_tile, void *stream);
@@ -239,7 +243,7 @@ xs_status xs_set_workspace(void *ws, unsigned long long bytes, void *stream);
  * unlimited workspace: *bytes = the workspace it would use and *cut = 1 if it
  * would take the balanced schedule (*bytes = 0 and *cut = 0 for whole units).
  * cut may be NULL. XS_ERR_INVALID for a NULL bytes or B, N, H < 0;
- * XS_ERR_UNSUPPORTED for d not in {64, 128} or N % 128 != 0; XS_ERR_CUDA if
+ * XS_ERR_UNSUPPORTED for d not in {64, 128, 256} or N % 128 != 0; XS_ERR_CUDA if
  * the device cannot be queried. */
 xs_status xs_workspace_bytes(int B, int N, int H, int d, unsigned long long *bytes, int *cut);
 
