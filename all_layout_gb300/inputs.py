@@ -48,6 +48,8 @@ WORKLOADS = {
     "peaked_16k": Workload("peaked B1 N16384 H24 d128 P8 q*4", 1, 16384, 24, 128, 8,
                            seed=3, q_scale=4.0),
     "video_dit": Workload("video-DiT B1 N65536 H24 d128 P8", 1, 65536, 24, 128, 8, seed=4),
+    # Head dimension 64 at twice the heads (48 x 64 = 24 x 128), a sweep shape.
+    "d64_16k": Workload("d64 B1 N16384 H48 d64 P8", 1, 16384, 48, 64, 8, seed=7),
     # Head dimension 256 at the same model width (12 heads x 256 = 24 x 128).
     "wide_4k": Workload("wide B1 N4096 H12 d256 P8", 1, 4096, 12, 256, 8, seed=5),
     "wide_16k": Workload("wide B1 N16384 H12 d256 P8", 1, 16384, 12, 256, 8, seed=6),

@@ -37,7 +37,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # so its traffic grows in proportion to B*N*H*d.
 PROFILE_FILES = {"image_dit": ("ncu_attn_fused_image_dit.md", "image_dit"),
                  "peaked_16k": ("ncu_attn_fused_peaked_16k.md", "peaked_16k"),
-                 "video_dit": ("ncu_attn_fused_peaked_16k.md", "peaked_16k")}
+                 "video_dit": ("ncu_attn_fused_peaked_16k.md", "peaked_16k"),
+                 "d64_16k": ("ncu_attn_fused_d64_16k.md", "d64_16k"),
+                 "wide_16k": ("ncu_attn_wide_d256_16k.md", "wide_16k")}
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -325,7 +327,8 @@ def run_xs(args, w, rank, world, local):
                 "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak)),
                 "traffic": traffic, "traffic_source": traffic_how,
                 "algorithmic_bytes": 4 * w.B * w.H * w.N * w.d * 2,
-                "kernel": "attn_kernel<%d> (fused)" % w.d,
+                "kernel": ("attn_wide_kernel (fused, d 256)" if w.d == 256 else
+                           "attn_kernel<%d> (fused)" % w.d),
                 "kernel_sha": kernel_sha()}
 
     cpu = None
