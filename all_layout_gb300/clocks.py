@@ -74,6 +74,16 @@ class ClockSampler:
         return summarize([line for ts, line in self.lines if t0 <= ts <= t1])
 
 
+def summary_near(stamped, t0: float, t1: float) -> dict:
+    """Clock record of the (time, line) samples taken between t0 and t1; a region
+    shorter than the sampling period takes the sample nearest to its middle."""
+    inside = [line for ts, line in stamped if t0 <= ts <= t1]
+    if not inside and stamped:
+        mid = 0.5 * (t0 + t1)
+        inside = [min(stamped, key=lambda e: abs(e[0] - mid))[1]]
+    return summarize(inside)
+
+
 def summarize(lines) -> dict:
     """Parse nvidia-smi CSV lines (the FIELDS order) into the clocks record."""
     sm, mx, reasons = [], None, set()

@@ -85,14 +85,17 @@ def sweep(Ns=(1024, 2048, 4096, 8192, 16384, 32768, 65536), balanced: bool = Tru
         if need:
             ws = torch.empty(need, dtype=torch.uint8, device="cuda")
             xs.set_workspace(ws)
-    rows = []
-    with clocks.ClockSampler(clocks.physical_gpu_index(torch.cuda.current_device())) as clk:
+    rows, spans = [], []
+    with clocks.ClockSampler(clocks.physical_gpu_index(torch.cuda.current_device()),
+                             period_ms=50) as clk:
         for N in Ns:
             t0 = time.time()
             r = measure(N, reps=5 if N >= 32768 else 10, **kw)
-            r["clocks"] = clk.summary(t0, time.time())
+            spans.append((t0, time.time()))
             r["stream_k"] = int(ws is not None and xs.workspace_bytes(1, N, r["H"], r["d"])[1])
             rows.append(r)
+    for r, (t0, t1) in zip(rows, spans):
+        r["clocks"] = clocks.summary_near(clk.lines, t0, t1)
     if ws is not None:
         xs.set_workspace(None)
     x = np.array([r["N"] for r in rows], dtype=np.float64)
@@ -115,7 +118,8 @@ def markdown(rep: dict, command: str) -> str:
            "`coupled` = `xs_attn_fused_ex` with XS_FLAG_COMPLETION_COUPLED (each issuing warp waits for",
            "its stores to complete, the pages' counterfactual). Span = per-tile store-issue span (first",
            "slab issued -> last issuing warp released). SM clock: median of the nvidia-smi samples",
-           f"taken while that N ran. kernel_sha: {kernel_sha()}", "",
+           "taken while that N ran (the nearest sample when it ran shorter than the 50 ms period).",
+           f"kernel_sha: {kernel_sha()}", "",
            "| N | stream-K | T_attn ms | T_fused ms | T_coupled ms | E_res/T_attn fused | "
            "E_res/T_attn coupled | span p50 / p99 (fused) | SM MHz | throttle reasons |",
            "|---|---|---|---|---|---|---|---|---|---|"]

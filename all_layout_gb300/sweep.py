@@ -45,16 +45,6 @@ def _time_ms(fns, reps, flush):
     return [float(np.median(t)) for t in ts]
 
 
-def _clocks_near(lines, t0, t1):
-    """Clock record of the samples taken between t0 and t1; a point shorter than
-    the sampling period takes the sample nearest to its middle."""
-    inside = [line for ts, line in lines if t0 <= ts <= t1]
-    if not inside and lines:
-        mid = 0.5 * (t0 + t1)
-        inside = [min(lines, key=lambda e: abs(e[0] - mid))[1]]
-    return clocks.summarize(inside)
-
-
 def run(points=None, reps: int = 7, balanced: bool = True):
     """Times every point; with `balanced`, a workspace is registered so that each
     launch may take the stream-K schedule (the same for all three paths)."""
@@ -90,7 +80,7 @@ def run(points=None, reps: int = 7, balanced: bool = True):
                          "tflops_fused": w.flops / (t_f * 1e-3) / 1e12,
                          "serial_over_fused": t_s / t_f, "fused_over_attn": t_f / t_a})
     for r, (t0, t1) in zip(rows, spans):
-        r["clocks"] = _clocks_near(clk.lines, t0, t1)
+        r["clocks"] = clocks.summary_near(clk.lines, t0, t1)
     if ws is not None:
         xs.set_workspace(None)
     return rows

@@ -82,3 +82,21 @@ def test_roofline_traffic_only_for_the_profiled_launch():
         assert bench.profiled_traffic(key, 4, True)[0] is None
         assert bench.profiled_traffic(key, 8, False)[0] is None
     assert bench.profiled_traffic("small", 8, True)[0] is None
+
+
+def test_clock_records():
+    """Clock summaries: median SM clock, reasons seen, nearest sample for short
+    regions, and the acceptance rule (hw/thermal reasons reject; sw_power_cap is
+    kept; a clock far below max with no reason rejects)."""
+    from all_layout_gb300 import clocks
+    line = lambda sm, reasons=(): ", ".join([str(sm), "2070", "900.0", "0x0"] + [
+        "Active" if r in reasons else "Not Active" for r in clocks.REASONS])
+    rec = clocks.summarize([line(2070), line(1900, ("sw_power_cap",)), line(1800)])
+    assert rec == {"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert clocks.accepted(rec)
+    assert not clocks.accepted(clocks.summarize([line(2070, ("hw_slowdown",))]))
+    assert not clocks.accepted(clocks.summarize([line(1200), line(1210)]))
+    stamped = [(1.0, line(2000)), (2.0, line(1500)), (3.0, line(1000))]
+    assert clocks.summary_near(stamped, 1.9, 2.05)["sm_mhz"] == 1500.0
+    assert clocks.summary_near(stamped, 2.4, 2.45)["sm_mhz"] == 1500.0    # nearest to 2.425
+    assert clocks.summary_near(stamped, 0.5, 3.5)["samples"] == 3
