@@ -52,8 +52,9 @@ def parse_args():
     ap.add_argument("--workload", default="video_dit",
                     help="one of all_layout_gb300.inputs.WORKLOADS (default: video-DiT N=65536)")
     ap.add_argument("--store-tile", type=int, default=None)
-    ap.add_argument("--side-steps", type=int, default=100,
-                    help="steps for the attention-alone / serial / scatter side timings")
+    ap.add_argument("--side-steps", type=int, default=30,
+                    help="rounds of the interleaved fused / attention-alone / serial / layout "
+                         "side timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--whole-units", action="store_true",
@@ -246,13 +247,20 @@ def run_xs(args, w, rank, world, local):
     value = flops * world / (ms_per_step * 1e-3) / 1e12
     clock_rec = clk.summary(t0, t1)
 
-    # Side timings on the same GPU: attention alone, serial path, layout kernel alone.
+    # Side timings on the same GPU: fused, attention alone, serial path and the
+    # layout kernel alone, one call of each per round, so that a clock that drifts
+    # over the run (the power cap engaging) biases none of the ratios.
     side = max(5, args.side_steps)
-    t_attn = sorted(timed(lambda: xs.attn(q, k, v, o, stream=stream), side))
-    t_serial = sorted(timed(lambda: xs.attn_serial(q, k, v, o, shards, stream=stream), side))
-    t_scatter = sorted(timed(lambda: xs.scatter(o, shards, stream=stream), side))
+    side_fns = (fused, lambda: xs.attn(q, k, v, o, stream=stream),
+                lambda: xs.attn_serial(q, k, v, o, shards, stream=stream),
+                lambda: xs.scatter(o, shards, stream=stream))
+    side_ms = [[] for _ in side_fns]
+    for _ in range(side):
+        for i, fn in enumerate(side_fns):
+            side_ms[i].append(timed(fn, 1)[0])
+    t_fused_side, t_attn, t_serial, t_scatter = (sorted(t) for t in side_ms)
     med = lambda a: a[len(a) // 2]
-    t_fused_med = med(sorted(step_ms))
+    t_fused_med = med(t_fused_side)
 
     # End to end through the public API with host buffers: every step copies its
     # q, k, v from pinned host memory, runs the fused call and reads every shard
