@@ -283,7 +283,10 @@ __device__ void softmax_role_w(const AttnParams &p, uint8_t *smem, WBars *bars, 
       }
       const float neg_m = -m;
       const uint64_t scale2 = f2_pack(scale, scale), negm2 = f2_pack(neg_m, neg_m);
-      float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+      // The row sum as one packed fp32x2 accumulator: one add per pair of
+      // exponentials instead of two (measured +1.4% at N = 16384, +2.6% at 4096;
+      // the two-tile kernel spills with it and keeps scalar sums).
+      uint64_t lsum2 = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -294,12 +297,14 @@ __device__ void softmax_role_w(const AttnParams &p, uint8_t *smem, WBars *bars, 
           float x0, x1;
           f2_unpack(x2, x0, x1);
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          lsum[i & 3] += p0 + p1;
+          lsum2 = f2_add(lsum2, f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + 16 * c, pk);
       }
-      l = fmaf(l, alpha, (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
+      float la, lb;
+      f2_unpack(lsum2, la, lb);
+      l = fmaf(l, alpha, la + lb);
       if (j > 0) {
         // Every step observes PV(gs - 1), the phase of pv_done before the one
         // this step's arrival enables. The wait is exact: S(gs) arrived after
