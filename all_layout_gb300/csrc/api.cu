@@ -139,6 +139,8 @@ xs_status validate(const void *const *ptrs, int nptrs, void *const *shards, int 
   // d = 256 stores each finished tile at once (no room to stage a deferred one).
   if (d == 256 && store_tile != 8) return XS_ERR_UNSUPPORTED;
   if (N % xs::kTileRows != 0) return XS_ERR_UNSUPPORTED;
+  // Row coordinates of the tensor maps (b*H + h)*N + n are 32-bit.
+  if (static_cast<long long>(B) * H * N > 0x7fffffffLL) return XS_ERR_UNSUPPORTED;
   for (int i = 0; i < nptrs; ++i)
     if (!aligned16(ptrs[i])) return XS_ERR_ALIGN;
   if (shards)

@@ -44,10 +44,11 @@
  *      XS_ERR_INVALID     a NULL pointer (also any NULL shard), B, N or H < 0,
  *                         P not in [1, 8], N % P != 0,
  *                         store_tile not in {1, 2, 4, 8};
- *      XS_ERR_UNSUPPORTED d not in {64, 128, 256}, N % 128 != 0, or d = 256
+ *      XS_ERR_UNSUPPORTED d not in {64, 128, 256}, N % 128 != 0, d = 256
  *                         with store_tile != 8 (at d = 256 every finished tile
  *                         is stored at once: a deferred tile does not fit on
- *                         chip beside the K/V ring);
+ *                         chip beside the K/V ring), or B*H*N >= 2^31 (the
+ *                         kernels address rows with 32-bit coordinates);
  *      XS_ERR_ALIGN       a pointer that is not 16-byte aligned.
  *    B == 0, H == 0 or N == 0 is an empty problem: the call validates its
  *    other arguments and returns XS_OK without launching anything.

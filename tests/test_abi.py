@@ -53,6 +53,7 @@ def _fused(xs, q=A, k=A, v=A, shards=(A, A), B=1, N=256, H=4, d=64, P=None, st=8
     (dict(st=3), 1), (dict(st=0), 1), (dict(st=16), 1),
     (dict(d=96), 2), (dict(d=512), 2), (dict(d=256, st=2), 2), (dict(d=256, st=1), 2),
     (dict(N=200, shards=(A, A)), 2),
+    (dict(B=1 << 10, H=1 << 14, N=1 << 7, shards=(A, A)), 2),    # B*H*N = 2^31 rows
     (dict(q=A + 8), 3), (dict(v=A + 2), 3), (dict(shards=(A, A + 4)), 3),
     (dict(B=0), 0), (dict(H=0), 0), (dict(N=0), 0),
 ])

@@ -359,3 +359,39 @@ def test_same_addresses_new_shapes_and_many_buffers(xs):
     torch.cuda.synchronize()
     for (_, _, _, shards) in keep[::13]:
         assert_close(shards_f64(shards), ref, "many buffers")
+
+
+# ------------------------------------------------------------------ more shapes
+
+def test_many_batches_many_waves(xs):
+    """B = 8 short sequences: 96 units over the persistent CTAs, each unit's tiles
+    in a different batch row block of the destinations."""
+    B, H, N, d, P = 8, 3, 256, 128, 4
+    q, k, v = inputs.qkv(B, N, H, d, seed=307)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    for st in (1, 8):
+        assert_close(shards_f64(_run_fused(xs, q, k, v, P, st)), ref, f"B=8 st={st}")
+
+
+def test_very_peaked_rows(xs):
+    """q x 16 (score std 16 in natural-log units): the running maximum jumps by far
+    more than the 2^8 rescale threshold within a row, and most weights underflow."""
+    B, H, N, d, P = 1, 2, 1024, 64, 2
+    q, k, v = inputs.qkv(B, N, H, d, seed=311, q_scale=16.0)
+    assert_close(shards_f64(_run_fused(xs, q, k, v, P)),
+                 oracle.shard_layout(oracle.attention(q, k, v), P), "q x 16")
+
+
+def test_ulysses_d64(xs):
+    B, Ht, N, d, P, ranks = 2, 4, 512, 64, 4, 2
+    q, k, v = inputs.qkv(B, N, Ht, d, seed=313)
+    qs, ks, vs = _seq_shards(q, P), _seq_shards(k, P), _seq_shards(v, P)
+    out = xs.alloc_shards(B, N, Ht, d, P)
+    for o in out:
+        o.fill_(float("nan"))
+    per = Ht // ranks
+    for r in range(ranks):
+        xs.attn_ulysses(qs, ks, vs, out, h0=r * per, H=per, store_tile=4)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    assert_close(shards_f64(out), oracle.shard_layout(oracle.attention(q, k, v), P), "ulysses d64")

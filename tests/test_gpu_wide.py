@@ -191,3 +191,33 @@ def test_wide_validation(xs):
     pp = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
     for st in (1, 2, 4):
         assert lib.xs_attn_fused(A, A, A, pp, 1, 256, 4, D, 2, st, None) == xs.ERR_UNSUPPORTED
+
+
+def test_wide_streamk_ulysses_and_spans(xs, ws):
+    """d = 256 under the balanced schedule: both All-to-Alls fused (two ranks' head
+    shares read from sequence shards) and fused_ex spans over tiles cut into pieces
+    that merge on another CTA."""
+    B, Ht, N, P, ranks = 1, 4, 2816, 2, 2
+    per = Ht // ranks
+    assert xs.workspace_bytes(B, N, per, D)[1] == 1
+    q, k, v = inputs.qkv(B, N, Ht, D, seed=251)
+    qs, ks, vs = _seq_shards(q, P), _seq_shards(k, P), _seq_shards(v, P)
+    out = xs.alloc_shards(B, N, Ht, D, P)
+    for o in out:
+        o.fill_(float("nan"))
+    for r in range(ranks):
+        xs.attn_ulysses(qs, ks, vs, out, h0=r * per, H=per, store_tile=8)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    assert_close(shards_f64(out), ref, "d256 ulysses stream-K")
+    # fused_ex on the same problem as one call: spans recorded for every tile
+    out2 = xs.alloc_shards(B, N, Ht, D, P)
+    n_tiles = B * Ht * (N // 128)
+    spans = torch.zeros(2 * n_tiles, dtype=torch.int64, device="cuda")
+    xs.attn_fused_ex(*_dev(q, k, v), out2, store_tile=8, flags=xs.FLAG_COMPLETION_COUPLED, spans=spans)
+    torch.cuda.synchronize()
+    assert xs.last_device_status() == xs.OK
+    assert_close(shards_f64(out2), ref, "d256 fused_ex stream-K")
+    t = spans.view(n_tiles, 2).cpu().numpy()
+    assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])
