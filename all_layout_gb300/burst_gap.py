@@ -19,16 +19,19 @@ through xs_store_burst_probe:
 CTA issues store_tile slabs of 16 output rows per KV iteration, and the
 iteration's compute is the gap.
 
-Run as ``python -m all_layout_gb300.burst_gap`` for a JSON report.
+Run as ``python -m all_layout_gb300.burst_gap [--markdown FILE]`` for a JSON
+report (SM clocks and throttle reasons sampled during each mode's run).
 """
 from __future__ import annotations
 
 import json
+import sys
+import time
 
 import numpy as np
 import torch
 
-from . import xs
+from . import clocks, xs
 
 MODES = {"posted": 0, "tma": 1}
 
@@ -133,6 +136,49 @@ def calibrate(K: int | None = None, mode: str = "posted", d: int = 128,
             "store_tile": choose_store_tile(T0, R, Q, K, slab, gap)}
 
 
+def calibrate_all() -> dict:
+    """Both store modes, each with the clock record of its run."""
+    rep = {}
+    with clocks.ClockSampler(clocks.physical_gpu_index(torch.cuda.current_device())) as clk:
+        for m in MODES:
+            t0 = time.time()
+            rep[m] = calibrate(mode=m)
+            rep[m]["clocks"] = (t0, time.time())
+    for m in rep:
+        rep[m]["clocks"] = clocks.summary_near(clk.lines, *rep[m]["clocks"])
+    return rep
+
+
+def markdown(rep: dict, command: str) -> str:
+    us = lambda s: f"{s * 1e6:.2f} us"
+    out = ["# Local Burst-Gap calibration (stores into this GB300's own HBM)", "",
+           f"Command (repository root): `{command}` (probe: `xs_store_burst_probe`,",
+           f"K = {rep['posted']['K']} producer CTAs of 128 threads; %globaltimer issue spans). The pages",
+           "calibrate remote NVLink stores on an eight-GPU node (R ~717 GB/s, T_iss^0 ~0.76 us at",
+           "K=148, B=32 KB, Q ~4.25 MiB); these are the single-GPU analogs.", "",
+           "| mode | T_iss^0 (32 KiB per producer) | R | Q (isolated-burst knee) | store_tile chosen "
+           "(gap 1.8 us) | SM MHz (median, reasons) |",
+           "|---|---|---|---|---|---|"]
+    for m, r in rep.items():
+        c = r["clocks"]
+        out.append(f"| {m} | {us(r['T0_s'])} | {r['R_bytes_per_s'] / 1e9:.0f} GB/s | "
+                   f"{r['Q_bytes'] / 2**20:.2f} MiB | {r['store_tile']} | "
+                   f"{c['sm_mhz'] or '-'}, {', '.join(c['reasons']) or 'none'} |")
+    out += ["", "Max law, steady-state issue span of periodic bursts (per producer B, aggregate "
+            "V = K B):", "", "| mode | B per producer | gap | measured | max(T0(V), V/R - G) |",
+            "|---|---|---|---|---|"]
+    for m, r in rep.items():
+        for B, rows in zip(("64 KiB", "256 KiB", "1 MiB"), r["max_law"]):
+            for row in rows:
+                out.append(f"| {m} | {B} | {row['gap_s'] * 1e6:.0f} us | {us(row['measured_s'])} | "
+                           f"{us(row['model_s'])} |")
+    return "\n".join(out) + "\n"
+
+
 if __name__ == "__main__":
-    rep = {m: calibrate(mode=m) for m in MODES}
+    rep = calibrate_all()
+    args = sys.argv[1:]
+    if "--markdown" in args:
+        with open(args[args.index("--markdown") + 1], "w") as f:
+            f.write(markdown(rep, "python -m all_layout_gb300.burst_gap"))
     print(json.dumps(rep, indent=1))
