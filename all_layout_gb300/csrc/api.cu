@@ -210,24 +210,36 @@ bool encode(CUtensorMap *m, void *base, int rank, const cuuint64_t *dims,
   return true;
 }
 
-// q/k/v: 3-D {d, N, B*H}, box {64, 128, 1}.
-bool encode_qkv(CUtensorMap *m, const void *base, int B, int N, int H, int d) {
+// q/k/v: 3-D {d, N, B*H}, box {64, box_rows, 1} (128 rows, or the keys of one KV
+// step of the single-tile kernel for K and V).
+bool encode_qkv(CUtensorMap *m, const void *base, int B, int N, int H, int d,
+                int box_rows = xs::kTileRows) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(B) * H};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(xs::kTileRows), 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   return encode(m, const_cast<void *>(base), 3, dims, strides, box);
 }
 
-// A sequence shard [B][rows][H_total][d] as 3-D {d, H_total, B*rows}, box {64, 1, 128}:
-// one box is 128 consecutive rows of one head.
-bool encode_seq_shard(CUtensorMap *m, const void *base, int B, int rows, int H_total, int d) {
+// A sequence shard [B][rows][H_total][d] as 3-D {d, H_total, B*rows}, box {64, 1,
+// box_rows}: one box is box_rows consecutive rows of one head.
+bool encode_seq_shard(CUtensorMap *m, const void *base, int B, int rows, int H_total, int d,
+                      int box_rows = xs::kTileRows) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H_total),
                               static_cast<cuuint64_t>(B) * rows};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(H_total) * d * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(xs::kTileRows)};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   return encode(m, const_cast<void *>(base), 3, dims, strides, box);
+}
+
+// Which kernel a launch takes: the single-tile kernel with double-buffered
+// scores at d = 256 (two tiles do not fit Tensor Memory), and at d = 64 for the
+// whole-tile store (store_tile 8) when kD64SingleTile is set; the two-tile
+// kernel otherwise.
+constexpr bool kD64SingleTile = false;
+bool single_tile(int d, int store_tile) {
+  return d == 256 || (kD64SingleTile && d == 64 && store_tile == 8);
 }
 
 // Destination rows: 2-D {cols, rows}, row pitch cols*2 bytes, box {64, 16}.
@@ -252,18 +264,20 @@ xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B
   xs::AttnParams prm;
   std::memset(&prm, 0, sizeof(prm));
   const int R = N / P;
+  const bool wide = single_tile(d, store_tile);
+  const int kv_rows = wide ? xs::wide_keys_per_step(d) : xs::kTileRows;   // keys per KV step
   if (!in.seq_shards) {
     if (!encode_qkv(&prm.tm_q[0], in.q[0], B, N, H, d) ||
-        !encode_qkv(&prm.tm_k[0], in.k[0], B, N, H, d) ||
-        !encode_qkv(&prm.tm_v[0], in.v[0], B, N, H, d))
+        !encode_qkv(&prm.tm_k[0], in.k[0], B, N, H, d, kv_rows) ||
+        !encode_qkv(&prm.tm_v[0], in.v[0], B, N, H, d, kv_rows))
       return XS_ERR_CUDA;
     prm.in_mode = 0;
     prm.in_rows = N;
   } else {
     for (int p = 0; p < P; ++p)
       if (!encode_seq_shard(&prm.tm_q[p], in.q[p], B, R, in.H_total, d) ||
-          !encode_seq_shard(&prm.tm_k[p], in.k[p], B, R, in.H_total, d) ||
-          !encode_seq_shard(&prm.tm_v[p], in.v[p], B, R, in.H_total, d))
+          !encode_seq_shard(&prm.tm_k[p], in.k[p], B, R, in.H_total, d, kv_rows) ||
+          !encode_seq_shard(&prm.tm_v[p], in.v[p], B, R, in.H_total, d, kv_rows))
         return XS_ERR_CUDA;
     prm.in_mode = 1;
     prm.in_rows = R;
@@ -293,18 +307,20 @@ xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B
   prm.coupled = coupled;
   prm.spans = spans;
   prm.shared_staging = store_tile == 8 ? 1 : 0;
-  prm.kv_stages = d == 256 ? 0 : xs::attn_kv_stages(d, store_tile == 8);
+  prm.kv_stages = wide ? 0 : xs::attn_kv_stages(d, store_tile == 8);
   prm.n_qtiles = N / xs::kTileRows;
-  // d <= 128: a unit is a pair of query tiles; d = 256: a single tile.
-  prm.n_pairs = d == 256 ? prm.n_qtiles : (prm.n_qtiles + 1) / 2;
+  // Two-tile kernel: a unit is a pair of query tiles; single-tile kernel: one tile.
+  prm.n_pairs = wide ? prm.n_qtiles : (prm.n_qtiles + 1) / 2;
   prm.n_units = B * H * prm.n_pairs;
-  prm.n_kv = N / xs::kTileRows;
+  prm.n_kv = N / kv_rows;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   prm.wait_limit_ns = g_wait_limit_ns.load();
   const int sms = sm_count();
   if (sms <= 0) return XS_ERR_CUDA;
   const Workspace ws = current_workspace();
-  const Plan pl = plan_launch(prm.n_units, sms, prm.n_kv, d, ws.ptr ? ws.bytes : 0);
+  // Persistent CTAs: one per SM, or the single-tile kernel's CTAs per SM.
+  const int slots = sms * (wide ? xs::wide_ctas_per_sm(d) : 1);
+  const Plan pl = plan_launch(prm.n_units, slots, prm.n_kv, d, ws.ptr ? ws.bytes : 0);
   const int grid = pl.grid;
   prm.sk = pl.sk;
   prm.sk_waves = pl.sk_waves;
@@ -313,7 +329,9 @@ xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B
     prm.ws_count = static_cast<int *>(ws.ptr);
     prm.ws_part = reinterpret_cast<float *>(static_cast<char *>(ws.ptr) + XS_WORKSPACE_HEADER_BYTES);
   }
-  return xs::launch_attn(prm, d, grid, stream) == cudaSuccess ? XS_OK : XS_ERR_CUDA;
+  const cudaError_t e = wide ? xs::launch_attn_wide(prm, d, grid, stream)
+                            : xs::launch_attn(prm, d, grid, stream);
+  return e == cudaSuccess ? XS_OK : XS_ERR_CUDA;
 }
 
 xs_status launch_layout(const void *o, void *const *shards, int B, int N, int H, int d, int P,
@@ -507,11 +525,19 @@ XS_API xs_status xs_workspace_bytes(int B, int N, int H, int d, unsigned long lo
   const int sms = sm_count();
   if (sms <= 0) return XS_ERR_CUDA;
   const int n_qtiles = N / xs::kTileRows;
-  // d <= 128: a unit is a pair of query tiles; d = 256: a single tile.
-  const int units = B * H * (d == 256 ? n_qtiles : (n_qtiles + 1) / 2);
-  const Plan pl = plan_launch(units, sms, n_qtiles, d, ~0ull);
+  // The store_tile 8 launch, and at d = 64 with the single-tile kernel also the
+  // two-tile kernel that store_tile < 8 takes: the larger workspace covers both.
+  const bool wide = single_tile(d, 8);
+  const int kv_rows = wide ? xs::wide_keys_per_step(d) : xs::kTileRows;
+  const int units = B * H * (wide ? n_qtiles : (n_qtiles + 1) / 2);
+  const Plan pl = plan_launch(units, sms * (wide ? xs::wide_ctas_per_sm(d) : 1), N / kv_rows, d,
+                              ~0ull);
   *bytes = pl.bytes;
   if (cut) *cut = pl.sk;
+  if (wide && d != 256) {
+    const Plan pair = plan_launch(B * H * ((n_qtiles + 1) / 2), sms, n_qtiles, d, ~0ull);
+    if (pair.bytes > *bytes) *bytes = pair.bytes;
+  }
   return XS_OK;
 }
 

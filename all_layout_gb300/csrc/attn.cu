@@ -1044,8 +1044,26 @@ cudaError_t launch_exp2_selftest(const float *x, float *out_poly, float *out_muf
 }
 
 int attn_smem_bytes(int d) {
-  if (d == 256) return wide::SMEM;
+  if (d == 256) return wide::Cfg256::SMEM;
   return d == 128 ? Cfg<128, false>::SMEM : Cfg<64, false>::SMEM;
+}
+
+int wide_keys_per_step(int d) { return d == 256 ? wide::Cfg256::BNW : wide::Cfg64::BNW; }
+int wide_ctas_per_sm(int d) { return d == 256 ? wide::Cfg256::CTAS : wide::Cfg64::CTAS; }
+
+template <class C>
+static cudaError_t launch_wide(const AttnParams &p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(wide::attn_wide_kernel<C>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  wide::attn_wide_kernel<C><<<grid, wide::kThreadsW, C::SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_wide(const AttnParams &p, int d, int grid, cudaStream_t s) {
+  if (d == 256) return launch_wide<wide::Cfg256>(p, grid, s);
+  if (d == 64) return launch_wide<wide::Cfg64>(p, grid, s);
+  return cudaErrorInvalidValue;
 }
 
 int attn_kv_stages(int d, bool shared_staging) {
@@ -1064,13 +1082,6 @@ static cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_attn(const AttnParams &p, int d, int grid, cudaStream_t s) {
-  if (d == 256) {
-    cudaError_t e = cudaFuncSetAttribute(wide::attn_wide_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, wide::SMEM);
-    if (e != cudaSuccess) return e;
-    wide::attn_wide_kernel<<<grid, wide::kThreadsW, wide::SMEM, s>>>(p);
-    return cudaGetLastError();
-  }
   const bool shared = p.shared_staging != 0;
   if (d == 128) return shared ? launch_one<128, true>(p, grid, s) : launch_one<128, false>(p, grid, s);
   return shared ? launch_one<64, true>(p, grid, s) : launch_one<64, false>(p, grid, s);

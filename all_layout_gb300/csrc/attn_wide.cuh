@@ -1,5 +1,6 @@
-// Head dimension 256: the same fused attention + shard store, one 128-row query
-// tile per CTA with S double-buffered in Tensor Memory.
+// One 128-row query tile per CTA with S double-buffered in Tensor Memory: the
+// kernel for head dimension 256, and a configuration of the same kernel for
+// head dimension 64 (64-key steps, two CTAs per SM).
 //
 // Included by attn.cu inside its anonymous namespace (it uses that file's
 // waits, loads, staging and slab stores).
@@ -11,36 +12,70 @@
 // V(j). Per KV step the tensor work is 2048 cycles (QK 1024, PV 1024) against
 // about 1450 for one row's softmax chain, so the pipe need not wait for it.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (192 threads; one CTA per SM at d = 256):
 //   warps 0-3  softmax, O rescale and epilogue (row r of the tile = TMEM lane r)
 //   warp 4     Tensor Memory allocation and the MMA issuer
 //   warp 5     TMA loader
-// Tensor Memory: S0 [0,128)  S1 [128,256)  O [256,512); P(j) (bf16 pairs)
-// overwrites the first 64 columns of S(j & 1).
-// Shared memory: Q (4 x 16 KiB halves of 64 columns) | K/V ring of 8 slots of
-// one 16 KiB half each: K(j) halves in slots 0-3, V(j) halves in slots 4-7, so
-// each half is released as soon as the MMAs reading it are done | four 8 KiB
-// one-slab staging buffers, one per softmax warp | barriers.
+// Tensor Memory (d = 256, 128-key steps): S0 [0,128)  S1 [128,256)  O [256,512);
+// P(j) (bf16 pairs) overwrites the first half of S(j & 1).
+// Shared memory: Q (64-column halves) | K/V ring of 64-column halves: K tiles in
+// KDEP groups of NH slots, then V tiles in VDEP groups, each half released as
+// soon as the MMAs reading it are done | four one-slab staging buffers, one per
+// softmax warp | barriers.
+//
+// The d = 64 configuration takes 64-key steps (S0 [0,64) S1 [64,128) O
+// [128,192), 256 columns allocated) so that two CTAs share an SM, each with its
+// own MMA issuer, and four K and four V tiles in flight.
 //
 // MMA order: QK(0); then per step j: QK(j+1) into S((j+1) & 1), PV(j). One
 // thread's tcgen05 operations execute in order, so QK(j+2) cannot overwrite
 // P(j) before PV(j) has read it.
 namespace wide {
 
-constexpr int D = 256;
-constexpr int NH = D / 64;                        // 64-column halves per row
 constexpr int kThreadsW = 192;
 constexpr int kMmaWarpW = 4;
 constexpr int kLoadWarpW = 5;
-constexpr int NSLOT = 2 * NH;                     // K halves 0..3, V halves 4..7
-constexpr int SLAB_BUF = kSlabRows * D * 2;       // 16 rows x 256 columns bf16
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + NH * kHalfBytes;
-constexpr int OFF_STG = OFF_KV + NSLOT * kHalfBytes;
-constexpr int OFF_BAR = OFF_STG + 4 * SLAB_BUF;
-constexpr int SMEM = OFF_BAR + 256 + 1024;        // + slack to align the base to 1024
-constexpr uint32_t COL_S = 0, COL_O = 256;
 
+// D: head dimension; BNW: keys per KV step; KDEP, VDEP: K and V tiles in flight;
+// PVN: columns of O per PV MMA; CTAS: CTAs per SM.
+template <int D_, int BNW_, int KDEP_, int VDEP_, int PVN_, int CTAS_>
+struct WCfg {
+  static constexpr int D = D_, BNW = BNW_, KDEP = KDEP_, VDEP = VDEP_, CTAS = CTAS_;
+  static constexpr int NH = D / 64;                  // 64-column halves of a row
+  static constexpr int PV_N = PVN_;
+  static constexpr int PV_HALVES = PV_N / 64;        // V halves one PV MMA reads
+  static constexpr int HALF_Q = BM * 128;            // one half of the 128-row Q tile
+  static constexpr int HALF_KV = BNW * 128;          // one half of a BNW-key K or V tile
+  static constexpr int NKS = KDEP * NH, NVS = VDEP * NH, NSLOT = NKS + NVS;
+  static constexpr int SLAB_BUF = kSlabRows * D * 2; // 16 rows x D columns bf16
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + NH * HALF_Q; // K slots, then V slots
+  static constexpr int OFF_STG = OFF_KV + NSLOT * HALF_KV;
+  static constexpr int OFF_BAR = OFF_STG + 4 * SLAB_BUF;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + slack to align the base to 1024
+  static constexpr uint32_t COL_S = 0, COL_O = 2 * BNW;
+  static constexpr uint32_t TMEM_COLS = 2 * BNW + D <= 256 ? 256 : 512;
+  static_assert(2 * BNW + D <= 512 && BNW % 32 == 0 && D % PV_N == 0, "layout");
+  static_assert(SMEM * CTAS <= 232448, "shared memory per SM");
+  // Slot of half hf of the K (V) tile of global step gs, and the parity of that
+  // slot's use by it.
+  static __device__ __forceinline__ int kslot(uint32_t gs, int hf) { return (gs % KDEP) * NH + hf; }
+  static __device__ __forceinline__ int vslot(uint32_t gs, int hf) {
+    return NKS + (gs % VDEP) * NH + hf;
+  }
+  static __device__ __forceinline__ uint32_t kpar(uint32_t gs) { return (gs / KDEP) & 1; }
+  static __device__ __forceinline__ uint32_t vpar(uint32_t gs) { return (gs / VDEP) & 1; }
+};
+
+// Head dimension 256: 128-key steps, one K and one V tile in flight (eight
+// 16 KiB halves), 128-column PV MMAs (64: 1451, 128: 1633, 256: 1539 TFLOP/s
+// at N = 16384), one CTA per SM.
+using Cfg256 = WCfg<256, 128, 1, 1, 128, 1>;
+// Head dimension 64: 64-key steps, four K and four V tiles in flight (8 KiB
+// each), 64-column PV MMAs, two CTAs per SM.
+using Cfg64 = WCfg<64, 64, 4, 4, 64, 2>;
+
+template <int NSLOT>
 struct WBars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
@@ -51,8 +86,7 @@ struct WBars {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(WBars) <= 256, "barrier block too large");
-static_assert(SMEM <= 232448, "shared memory of the d = 256 kernel");
+static_assert(sizeof(WBars<8>) <= 256, "barrier block too large");
 
 // The k-th item of this CTA's work list (get_item: whole units strided over the
 // persistent CTAs, or with a workspace, stream-K pieces of the last waves). A
@@ -69,8 +103,10 @@ __device__ __forceinline__ bool wide_item(const AttnParams &p, int k, Item &it, 
 // one phase before V(j-1) slots (PV(j-1) done), so the loader fills K one step
 // ahead of V: K(0), K(1), V(0), K(2), V(1), ... Loading K(j+1) behind V(j) would
 // leave QK(j+1) waiting a whole load latency every step.
-__device__ void load_role_w(const AttnParams &p, uint8_t *smem, WBars *bars,
+template <class C>
+__device__ void load_role_w(const AttnParams &p, uint8_t *smem, WBars<C::NSLOT> *bars,
                             volatile int *abort_flag) {
+  constexpr int NH = C::NH;
   const uint64_t lim = p.wait_limit_ns;
   const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
   auto wait = [&](uint32_t bar, uint32_t parity) {
@@ -78,17 +114,18 @@ __device__ void load_role_w(const AttnParams &p, uint8_t *smem, WBars *bars,
   };
   uint32_t lu = 0, q_armed = 0;
   uint32_t k_loads = 0, v_loads = 0;   // K and V tiles loaded (global steps)
-  uint32_t armed[NSLOT] = {};           // loads issued into each slot
-  // The four halves of K (kind 0) or V (kind 1) of key tile j, global step gs.
+  uint32_t armed[C::NSLOT] = {};        // loads issued into each slot
+  // The halves of K (kind 0) or V (kind 1) of key tile j, global step gs.
   auto load_kv = [&](int kind, int j, int bh, uint32_t gs) -> bool {
     for (int hf = 0; hf < NH; ++hf) {
-      const int s = kind * NH + hf;
-      if (!wait(smem_u32(&bars->kv_empty[s]), (gs & 1) ^ 1)) return false;
+      const int s = kind == 0 ? C::kslot(gs, hf) : C::vslot(gs, hf);
+      const uint32_t par = kind == 0 ? C::kpar(gs) : C::vpar(gs);
+      if (!wait(smem_u32(&bars->kv_empty[s]), par ^ 1)) return false;
       const uint32_t full = smem_u32(&bars->kv_full[s]);
       if (elect_one()) {
-        mbar_arrive_expect_tx(full, kHalfBytes);
-        load_tile(p, kind == 0 ? p.tm_k : p.tm_v, smem_u32(smem + OFF_KV + s * kHalfBytes), full,
-                  hf, j * BN, bh);
+        mbar_arrive_expect_tx(full, C::HALF_KV);
+        load_tile(p, kind == 0 ? p.tm_k : p.tm_v, smem_u32(smem + C::OFF_KV + s * C::HALF_KV),
+                  full, hf, j * C::BNW, bh);
       }
       __syncwarp();
       ++armed[s];
@@ -100,9 +137,9 @@ __device__ void load_role_w(const AttnParams &p, uint8_t *smem, WBars *bars,
   for (; wide_item(p, static_cast<int>(lu), item, bh, q0); ++lu) {
     if (lu > 0 && !wait(q_empty, (lu - 1) & 1)) goto drain;
     if (elect_one()) {
-      mbar_arrive_expect_tx(q_full, NH * kHalfBytes);
+      mbar_arrive_expect_tx(q_full, NH * C::HALF_Q);
       for (int hf = 0; hf < NH; ++hf)
-        load_tile(p, p.tm_q, smem_u32(smem + OFF_Q + hf * kHalfBytes), q_full, hf, q0, bh);
+        load_tile(p, p.tm_q, smem_u32(smem + C::OFF_Q + hf * C::HALF_Q), q_full, hf, q0, bh);
     }
     __syncwarp();
     ++q_armed;
@@ -120,31 +157,33 @@ __device__ void load_role_w(const AttnParams &p, uint8_t *smem, WBars *bars,
 drain:
   // Every load issued must land before the CTA releases its shared memory:
   // wait for the last phase armed on each slot.
-  for (int s = 0; s < NSLOT; ++s)
+  for (int s = 0; s < C::NSLOT; ++s)
     if (armed[s]) drain_phase(smem_u32(&bars->kv_full[s]), (armed[s] - 1) & 1, lim);
   if (q_armed > 0) drain_phase(q_full, (q_armed - 1) & 1, lim);
 }
 
 // S(b) = Q K^T for global step gs, one 64-column half of d at a time; each
 // K half is released when its four MMAs are done.
-__device__ __forceinline__ bool issue_qk_w(WBars *bars, uint32_t s_col, uint64_t qdesc,
+template <class C>
+__device__ __forceinline__ bool issue_qk_w(WBars<C::NSLOT> *bars, uint32_t s_col, uint64_t qdesc,
                                            uint64_t kdesc0, uint32_t gs, volatile int *abort_flag,
                                            uint64_t lim) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0);
-  for (int hf = 0; hf < NH; ++hf) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, C::BNW, 0);
+  for (int hf = 0; hf < C::NH; ++hf) {
+    const int ks = C::kslot(gs, hf);
     if (!__all_sync(0xffffffffu,
-                    wait_phase(smem_u32(&bars->kv_full[hf]), gs & 1, abort_flag, lim)))
+                    wait_phase(smem_u32(&bars->kv_full[ks]), C::kpar(gs), abort_flag, lim)))
       return false;
     tc_fence_after();
     if (elect_one()) {
-      const uint64_t kd = kdesc0 + static_cast<uint64_t>((hf * kHalfBytes) >> 4);
-      const uint64_t qd = qdesc + static_cast<uint64_t>((hf * kHalfBytes) >> 4);
+      const uint64_t kd = kdesc0 + static_cast<uint64_t>((ks * C::HALF_KV) >> 4);
+      const uint64_t qd = qdesc + static_cast<uint64_t>((hf * C::HALF_Q) >> 4);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
         tc_mma_ss(s_col, qd + off, kd + off, idesc, (hf > 0 || kk > 0) ? 1u : 0u);
       }
-      tc_commit(smem_u32(&bars->kv_empty[hf]));
+      tc_commit(smem_u32(&bars->kv_empty[ks]));
     }
     __syncwarp();
   }
@@ -153,34 +192,32 @@ __device__ __forceinline__ bool issue_qk_w(WBars *bars, uint32_t s_col, uint64_t
   return true;
 }
 
-// Columns of O per PV MMA. A 128 x 64 x 16 MMA took about 50 cycles against
-// 32 of tensor work (the per-instruction cost dominates); wider MMAs amortise
-// it, at the price of releasing more V halves at once. Measured at N = 16384
-// (4096), TFLOP/s: 64 columns 1451 (1180), 128 columns 1633 (1310), 256
-// columns 1539 (1078).
-constexpr int PV_N = 128;
-constexpr int PV_HALVES = PV_N / 64;   // V halves one PV MMA reads
-
-// O (+)= P(gs) V(gs): per group of PV_N columns of O, eight MMAs over 16 keys
-// each (V as the MN-major B operand, its 64-column halves kHalfBytes apart);
-// the group's V halves are released when its MMAs are done.
-__device__ __forceinline__ bool issue_pv_w(WBars *bars, uint32_t o_col, uint32_t p_col,
+// O (+)= P(gs) V(gs): per group of PV_N columns of O, one MMA per 16 keys (V as
+// the MN-major B operand, its 64-column halves HALF_KV apart in consecutive
+// slots); the group's V halves are released when its MMAs are done. A 128 x 64
+// x 16 MMA took about 50 cycles against 32 of tensor work (the per-instruction
+// cost dominates), so d = 256 uses 128-column MMAs.
+template <class C>
+__device__ __forceinline__ bool issue_pv_w(WBars<C::NSLOT> *bars, uint32_t o_col, uint32_t p_col,
                                            uint64_t vdesc0, uint32_t gs, bool first,
                                            volatile int *abort_flag, uint64_t lim) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, PV_N, 1);
-  for (int grp = 0; grp < NH / PV_HALVES; ++grp) {
-    for (int h = 0; h < PV_HALVES; ++h)
-      if (!__all_sync(0xffffffffu, wait_phase(smem_u32(&bars->kv_full[NH + grp * PV_HALVES + h]),
-                                              gs & 1, abort_flag, lim)))
+  constexpr uint32_t idesc = idesc_bf16_f32(128, C::PV_N, 1);
+  for (int grp = 0; grp < C::NH / C::PV_HALVES; ++grp) {
+    for (int h = 0; h < C::PV_HALVES; ++h)
+      if (!__all_sync(0xffffffffu,
+                      wait_phase(smem_u32(&bars->kv_full[C::vslot(gs, grp * C::PV_HALVES + h)]),
+                                 C::vpar(gs), abort_flag, lim)))
         return false;
     tc_fence_after();
     if (elect_one()) {
-      const uint64_t vd = vdesc0 + static_cast<uint64_t>((grp * PV_HALVES * kHalfBytes) >> 4);
+      const int vs = C::vslot(gs, grp * C::PV_HALVES);
+      const uint64_t vd = vdesc0 + static_cast<uint64_t>((vs * C::HALF_KV) >> 4);
 #pragma unroll
-      for (int ks = 0; ks < BN / 16; ++ks)
-        tc_mma_ts(o_col + grp * PV_N, p_col + ks * 8, vd + static_cast<uint64_t>((ks * 2048) >> 4),
-                  idesc, (!first || ks > 0) ? 1u : 0u);
-      for (int h = 0; h < PV_HALVES; ++h) tc_commit(smem_u32(&bars->kv_empty[NH + grp * PV_HALVES + h]));
+      for (int ks = 0; ks < C::BNW / 16; ++ks)
+        tc_mma_ts(o_col + grp * C::PV_N, p_col + ks * 8,
+                  vd + static_cast<uint64_t>((ks * 2048) >> 4), idesc, (!first || ks > 0) ? 1u : 0u);
+      for (int h = 0; h < C::PV_HALVES; ++h)
+        tc_commit(smem_u32(&bars->kv_empty[vs + h]));
     }
     __syncwarp();
   }
@@ -189,27 +226,30 @@ __device__ __forceinline__ bool issue_pv_w(WBars *bars, uint32_t o_col, uint32_t
   return true;
 }
 
-__device__ void mma_role_w(const AttnParams &p, uint8_t *smem, WBars *bars, uint32_t tmem_in,
-                           volatile int *abort_flag) {
+template <class C>
+__device__ void mma_role_w(const AttnParams &p, uint8_t *smem, WBars<C::NSLOT> *bars,
+                           uint32_t tmem_in, volatile int *abort_flag) {
   const uint64_t lim = p.wait_limit_ns;
   const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_in, 0);
   const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
-  const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
-  const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_KV), 16, 1024);
-  const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + OFF_KV + NH * kHalfBytes), kHalfBytes, 1024);
+  // Descriptors of the first Q half and of slot 0; a slot's start is added per MMA.
+  const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+  const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
+  const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + C::OFF_KV), C::HALF_KV, 1024);
   uint32_t lu = 0, g = 0;   // items and KV steps (global) issued
   Item item;
   int bh, q0;
   for (; wide_item(p, static_cast<int>(lu), item, bh, q0); ++lu) {
     const int nk = item.kv1 - item.kv0;
     if (!__all_sync(0xffffffffu, wait_phase(q_full, lu & 1, abort_flag, lim))) goto drain;
-    if (!issue_qk_w(bars, tmem + COL_S + (g & 1) * 128, qdesc, kdesc0, g, abort_flag, lim))
+    if (!issue_qk_w<C>(bars, tmem + C::COL_S + (g & 1) * C::BNW, qdesc, kdesc0, g, abort_flag,
+                       lim))
       goto drain;
     for (int j = 0; j < nk; ++j) {
       const uint32_t gs = g + j;
       if (j + 1 < nk) {
-        if (!issue_qk_w(bars, tmem + COL_S + ((gs + 1) & 1) * 128, qdesc, kdesc0, gs + 1,
-                        abort_flag, lim))
+        if (!issue_qk_w<C>(bars, tmem + C::COL_S + ((gs + 1) & 1) * C::BNW, qdesc, kdesc0, gs + 1,
+                           abort_flag, lim))
           goto drain;
       } else {
         if (elect_one()) tc_commit(q_empty);   // the unit's last QK has been issued
@@ -218,8 +258,8 @@ __device__ void mma_role_w(const AttnParams &p, uint8_t *smem, WBars *bars, uint
       if (!__all_sync(0xffffffffu, wait_phase(smem_u32(&bars->p_full), gs & 1, abort_flag, lim)))
         goto drain;
       tc_fence_after();
-      if (!issue_pv_w(bars, tmem + COL_O, tmem + COL_S + (gs & 1) * 128, vdesc0, gs, j == 0,
-                      abort_flag, lim))
+      if (!issue_pv_w<C>(bars, tmem + C::COL_O, tmem + C::COL_S + (gs & 1) * C::BNW, vdesc0, gs,
+                         j == 0, abort_flag, lim))
         goto drain;
     }
     g += nk;
@@ -230,15 +270,18 @@ drain:
   drain_phase(smem_u32(&bars->drain), 0, lim);
 }
 
-__device__ void softmax_role_w(const AttnParams &p, uint8_t *smem, WBars *bars, uint32_t tmem,
-                               volatile int *abort_flag) {
+template <class C>
+__device__ void softmax_role_w(const AttnParams &p, uint8_t *smem, WBars<C::NSLOT> *bars,
+                               uint32_t tmem, volatile int *abort_flag) {
+  constexpr int D = C::D;
+  constexpr int NC = C::BNW / 32;            // 32-column chunks of an S row
   const uint64_t lim = p.wait_limit_ns;
   const int wq = threadIdx.x / 32;           // TMEM lane quarter
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t tO = tmem + lane_base + COL_O;
+  const uint32_t tO = tmem + lane_base + C::COL_O;
   const uint32_t p_full = smem_u32(&bars->p_full), pv_done = smem_u32(&bars->pv_done);
-  uint8_t *slab_buf = smem + OFF_STG + wq * SLAB_BUF;
+  uint8_t *slab_buf = smem + C::OFF_STG + wq * C::SLAB_BUF;
   const float scale = p.scale_log2;
   uint32_t lu = 0, g = 0;
   Item item;
@@ -248,23 +291,27 @@ __device__ void softmax_role_w(const AttnParams &p, uint8_t *smem, WBars *bars, 
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < nk; ++j) {
       const uint32_t gs = g + j;
-      const uint32_t tS = tmem + lane_base + COL_S + (gs & 1) * 128;
+      const uint32_t tS = tmem + lane_base + C::COL_S + (gs & 1) * C::BNW;
       if (!__all_sync(0xffffffffu, wait_phase(smem_u32(&bars->s_full[gs & 1]), (gs >> 1) & 1,
                                                abort_flag, lim)))
         goto teardown;
       tc_fence_after();
-      uint32_t s[4][32];
+      uint32_t s[NC][32];
+      float mp[8];
       tmem_ld32(tS, s[0]);
       tmem_ld32(tS + 32, s[1]);
       tmem_wait_ld_regs(s[0]);
       tmem_wait_ld_regs(s[1]);
-      tmem_ld32(tS + 64, s[2]);
-      tmem_ld32(tS + 96, s[3]);
-      float mp[8];
+      if constexpr (NC == 4) {
+        tmem_ld32(tS + 64, s[2]);
+        tmem_ld32(tS + 96, s[3]);
+      }
       row_max_part(s[0], s[1], mp, true);
-      tmem_wait_ld_regs(s[2]);
-      tmem_wait_ld_regs(s[3]);
-      row_max_part(s[2], s[3], mp, false);
+      if constexpr (NC == 4) {
+        tmem_wait_ld_regs(s[2]);
+        tmem_wait_ld_regs(s[3]);
+        row_max_part(s[2], s[3], mp, false);
+      }
       const float mx = max3(max3(mp[0], mp[1], mp[2]), max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       const float m_new = fmaxf(m, mx * scale);
       float alpha = 1.f;
@@ -288,7 +335,7 @@ __device__ void softmax_role_w(const AttnParams &p, uint8_t *smem, WBars *bars, 
       // the two-tile kernel spills with it and keeps scalar sums).
       uint64_t lsum2 = f2_pack(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < NC; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -378,16 +425,17 @@ teardown:
   if (lane == 0) bulk_wait_all();
 }
 
-__global__ void __launch_bounds__(kThreadsW, 1) attn_wide_kernel(const __grid_constant__ AttnParams p) {
+template <class C>
+__global__ void __launch_bounds__(kThreadsW, C::CTAS) attn_wide_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  WBars *bars = reinterpret_cast<WBars *>(smem + OFF_BAR);
+  WBars<C::NSLOT> *bars = reinterpret_cast<WBars<C::NSLOT> *>(smem + C::OFF_BAR);
   volatile int *abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->q_full), 1);
     mbar_init(smem_u32(&bars->q_empty), 1);
-    for (int s = 0; s < NSLOT; ++s) {
+    for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(smem_u32(&bars->kv_full[s]), 1);
       mbar_init(smem_u32(&bars->kv_empty[s]), 1);
     }
@@ -401,7 +449,7 @@ __global__ void __launch_bounds__(kThreadsW, 1) attn_wide_kernel(const __grid_co
     fence_proxy_async_smem();
   }
   if (warp == kMmaWarpW) {
-    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_alloc(smem_u32(&bars->tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
   if (warp == kLoadWarpW && lane == 0) {
@@ -414,19 +462,19 @@ __global__ void __launch_bounds__(kThreadsW, 1) attn_wide_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   if (warp == kLoadWarpW) {
-    load_role_w(p, smem, bars, abort_flag);
+    load_role_w<C>(p, smem, bars, abort_flag);
     __syncwarp();
   } else if (warp == kMmaWarpW) {
-    mma_role_w(p, smem, bars, tmem, abort_flag);
+    mma_role_w<C>(p, smem, bars, tmem, abort_flag);
     __syncwarp();
   } else {
-    softmax_role_w(p, smem, bars, tmem, abort_flag);
+    softmax_role_w<C>(p, smem, bars, tmem, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarpW) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
