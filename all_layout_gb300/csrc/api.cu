@@ -234,13 +234,9 @@ bool encode_seq_shard(CUtensorMap *m, const void *base, int B, int rows, int H_t
 }
 
 // Which kernel a launch takes: the single-tile kernel with double-buffered
-// scores at d = 256 (two tiles do not fit Tensor Memory), and at d = 64 for the
-// whole-tile store (store_tile 8) when kD64SingleTile is set; the two-tile
-// kernel otherwise.
-constexpr bool kD64SingleTile = false;
-bool single_tile(int d, int store_tile) {
-  return d == 256 || (kD64SingleTile && d == 64 && store_tile == 8);
-}
+// scores at d = 256 (two tiles do not fit Tensor Memory), the two-tile kernel
+// otherwise.
+bool single_tile(int d) { return d == 256; }
 
 // Destination rows: 2-D {cols, rows}, row pitch cols*2 bytes, box {64, 16}.
 bool encode_rows(CUtensorMap *m, void *base, unsigned long long cols, unsigned long long rows) {
@@ -264,7 +260,7 @@ xs_status launch_attention(const Inputs &in, void *o, void *const *shards, int B
   xs::AttnParams prm;
   std::memset(&prm, 0, sizeof(prm));
   const int R = N / P;
-  const bool wide = single_tile(d, store_tile);
+  const bool wide = single_tile(d);
   const int kv_rows = wide ? xs::wide_keys_per_step(d) : xs::kTileRows;   // keys per KV step
   if (!in.seq_shards) {
     if (!encode_qkv(&prm.tm_q[0], in.q[0], B, N, H, d) ||
@@ -525,19 +521,13 @@ XS_API xs_status xs_workspace_bytes(int B, int N, int H, int d, unsigned long lo
   const int sms = sm_count();
   if (sms <= 0) return XS_ERR_CUDA;
   const int n_qtiles = N / xs::kTileRows;
-  // The store_tile 8 launch, and at d = 64 with the single-tile kernel also the
-  // two-tile kernel that store_tile < 8 takes: the larger workspace covers both.
-  const bool wide = single_tile(d, 8);
+  const bool wide = single_tile(d);
   const int kv_rows = wide ? xs::wide_keys_per_step(d) : xs::kTileRows;
   const int units = B * H * (wide ? n_qtiles : (n_qtiles + 1) / 2);
   const Plan pl = plan_launch(units, sms * (wide ? xs::wide_ctas_per_sm(d) : 1), N / kv_rows, d,
                               ~0ull);
   *bytes = pl.bytes;
   if (cut) *cut = pl.sk;
-  if (wide && d != 256) {
-    const Plan pair = plan_launch(B * H * ((n_qtiles + 1) / 2), sms, n_qtiles, d, ~0ull);
-    if (pair.bytes > *bytes) *bytes = pair.bytes;
-  }
   return XS_OK;
 }
 

@@ -1048,8 +1048,8 @@ int attn_smem_bytes(int d) {
   return d == 128 ? Cfg<128, false>::SMEM : Cfg<64, false>::SMEM;
 }
 
-int wide_keys_per_step(int d) { return d == 256 ? wide::Cfg256::BNW : wide::Cfg64::BNW; }
-int wide_ctas_per_sm(int d) { return d == 256 ? wide::Cfg256::CTAS : wide::Cfg64::CTAS; }
+int wide_keys_per_step(int) { return wide::Cfg256::BNW; }
+int wide_ctas_per_sm(int) { return wide::Cfg256::CTAS; }
 
 template <class C>
 static cudaError_t launch_wide(const AttnParams &p, int grid, cudaStream_t s) {
@@ -1062,7 +1062,6 @@ static cudaError_t launch_wide(const AttnParams &p, int grid, cudaStream_t s) {
 
 cudaError_t launch_attn_wide(const AttnParams &p, int d, int grid, cudaStream_t s) {
   if (d == 256) return launch_wide<wide::Cfg256>(p, grid, s);
-  if (d == 64) return launch_wide<wide::Cfg64>(p, grid, s);
   return cudaErrorInvalidValue;
 }
 

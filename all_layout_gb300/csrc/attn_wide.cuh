@@ -1,6 +1,5 @@
-// One 128-row query tile per CTA with S double-buffered in Tensor Memory: the
-// kernel for head dimension 256, and a configuration of the same kernel for
-// head dimension 64 (64-key steps, two CTAs per SM).
+// Head dimension 256: the same fused attention + shard store, one 128-row query
+// tile per CTA with S double-buffered in Tensor Memory.
 //
 // Included by attn.cu inside its anonymous namespace (it uses that file's
 // waits, loads, staging and slab stores).
@@ -23,9 +22,11 @@
 // soon as the MMAs reading it are done | four one-slab staging buffers, one per
 // softmax warp | barriers.
 //
-// The d = 64 configuration takes 64-key steps (S0 [0,64) S1 [64,128) O
-// [128,192), 256 columns allocated) so that two CTAs share an SM, each with its
-// own MMA issuer, and four K and four V tiles in flight.
+// The kernel is written over its configuration (WCfg below). A d = 64
+// configuration with 64-key steps (S0, S1 and O in 256 columns, two CTAs per
+// SM, each with its own issuer) was parity-green but 2-3% slower than the
+// two-tile kernel at d = 64 (N = 16384: 1088 against 1110 TFLOP/s; 32768: 1102
+// against 1131), so only the d = 256 configuration is built.
 //
 // MMA order: QK(0); then per step j: QK(j+1) into S((j+1) & 1), PV(j). One
 // thread's tcgen05 operations execute in order, so QK(j+2) cannot overwrite
@@ -71,9 +72,6 @@ struct WCfg {
 // 16 KiB halves), 128-column PV MMAs (64: 1451, 128: 1633, 256: 1539 TFLOP/s
 // at N = 16384), one CTA per SM.
 using Cfg256 = WCfg<256, 128, 1, 1, 128, 1>;
-// Head dimension 64: 64-key steps, four K and four V tiles in flight (8 KiB
-// each), 64-column PV MMAs, two CTAs per SM.
-using Cfg64 = WCfg<64, 64, 4, 4, 64, 2>;
 
 template <int NSLOT>
 struct WBars {

@@ -57,8 +57,8 @@ struct ShardPtrs {
 int attn_smem_bytes(int d);
 int attn_kv_stages(int d, bool shared_staging);
 cudaError_t launch_attn(const AttnParams &p, int d, int grid, cudaStream_t s);
-// The single-tile kernel with double-buffered scores (d = 256; d = 64 when it is
-// chosen): keys per KV step, CTAs per SM, launch.
+// The single-tile kernel with double-buffered scores (d = 256): keys per KV
+// step, CTAs per SM, launch.
 int wide_keys_per_step(int d);
 int wide_ctas_per_sm(int d);
 cudaError_t launch_attn_wide(const AttnParams &p, int d, int grid, cudaStream_t s);
