@@ -395,3 +395,40 @@ def test_ulysses_d64(xs):
     torch.cuda.synchronize()
     assert xs.last_device_status() == xs.OK
     assert_close(shards_f64(out), oracle.shard_layout(oracle.attention(q, k, v), P), "ulysses d64")
+
+
+# ------------------------------------------------------------------ host threads
+
+def test_concurrent_host_threads(xs):
+    """Eight host threads (the C-ABI call releases the interpreter lock) each launch
+    attention on their own stream with their own buffers: the tensor-map cache and
+    the launch path serve them at once, and every result matches the oracle."""
+    import threading
+    shapes = [(1, 2, 256 + 128 * (i % 4), 64 if i % 2 else 128, 2) for i in range(8)]
+    cases = []
+    for i, (B, H, N, d, P) in enumerate(shapes):
+        q, k, v = inputs.qkv(B, N, H, d, seed=500 + i)
+        cases.append((q, k, v, P, _dev(q, k, v), xs.alloc_shards(B, N, H, d, P)))
+    streams = [torch.cuda.Stream() for _ in cases]
+    errors = []
+
+    def run(i):
+        try:
+            torch.cuda.set_device(0)
+            _, _, _, P, (qd, kd, vd), shards = cases[i]
+            for _ in range(20):
+                xs.attn_fused(qd, kd, vd, shards, store_tile=8 if i % 3 else 2, stream=streams[i])
+        except Exception as e:          # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert xs.last_device_status() == xs.OK
+    for (q, k, v, P, _, shards) in cases:
+        assert_close(shards_f64(shards), oracle.shard_layout(oracle.attention(q, k, v), P),
+                     "concurrent host threads")
