@@ -18,11 +18,12 @@
 // (unit, KV tile) iterations (stream-K); a unit cut by a range boundary runs as
 // pieces whose partial results are merged on the GPU (get_item, finish_piece).
 //
-// Roles (320 threads, one CTA per SM):
+// Roles (320 threads at d = 128, 352 at d = 64; one CTA per SM):
 //   warps 0-3  softmax warp group 0: owns query tile 0 of the unit (S0, P0, O0)
 //   warps 4-7  softmax warp group 1: owns query tile 1 (S1, P1, O1)
-//   warp 8     MMA issuer + Tensor Memory allocation
+//   warp 8     MMA issuer + Tensor Memory allocation (d = 64: the QK^T issuer)
 //   warp 9     TMA loader
+//   warp 10    d = 64 only: the PV issuer
 // The issuer and loader warps run their control flow as whole warps (values stay
 // warp-uniform) and one elected lane issues each group of tcgen05 or TMA
 // operations.
@@ -35,17 +36,22 @@
 //
 // Tensor Memory (512 columns x 128 lanes, row r of a tile = lane r):
 //   S0 [0,128)  S1 [128,256)  O0 [256,256+d)  O1 [256+d,256+2d)
-//   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
+//   d = 128: P_t (bf16, two per column) overwrites the first 64 columns of S_t.
+//   d = 64:  P0 [384,448)  P1 [448,512), so S_t is free once it is read (EARLY_QK).
 // Shared memory (d = 128): Q0 Q1 | five 32 KiB regions: 4 K/V slots + 1 staging
 // tile cut into eight 4 KiB one-slab buffers, one per softmax warp (store_tile =
 // 8), or 3 K/V slots + 1 staging tile per group (store_tile < 8) | barriers. Every
 // tile is stored as 64-column halves of its rows x 128 bytes, 128-byte swizzle.
 //
-// MMA order per KV step j (t = 0, 1):  O_t += P_t(j-1) V(j-1);  S_t = Q_t K(j)^T.
-// tcgen05 operations issued by one thread execute in order, so S_t(j) cannot
-// overwrite P_t(j-1) before the PV MMA that reads it; and the commit that
-// signals S_t(j) also covers PV_t(j-1), so the softmax group may rescale O_t as
-// soon as it sees S_t(j).
+// MMA order per KV step j at d = 128 (t = 0, 1): O_t += P_t(j-1) V(j-1);
+// S_t = Q_t K(j)^T. tcgen05 operations issued by one thread execute in order, so
+// S_t(j) cannot overwrite P_t(j-1) before the PV MMA that reads it; and the
+// commit that signals S_t(j) also covers PV_t(j-1), so the softmax group may
+// rescale O_t as soon as it sees S_t(j).
+// At d = 64 (EARLY_QK) S_t(j+1) = Q_t K(j+1)^T is issued as soon as the group
+// has read S_t(j) into registers, by its own warp, and O_t += P_t(j) V(j) by
+// another once P_t(j) is written; the group waits for PV_t(j-1) (pv_done) before
+// it overwrites P_t or rescales O_t (qk_issuer, pv_issuer).
 #include <cstdint>
 
 #include "internal.h"
@@ -61,20 +67,22 @@ namespace {
 constexpr int BM = kTileRows;            // query rows per tile
 constexpr int BN = kTileRows;            // keys per KV tile
 constexpr int NSLAB = BM / kSlabRows;    // 8 slabs per output tile
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 8;    // the MMA issuer (with EARLY_QK: the QK^T issuer)
 constexpr int kLoadWarp = 9;
+constexpr int kPvWarp = 10;    // EARLY_QK only: the PV issuer
 constexpr int kHalfBytes = BM * 128;     // one 64-column half of a 128-row tile
 constexpr uint32_t kWaitSleepNs = 100000;   // longest suspension per try in a blocked wait
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 // Exponentials computed by the polynomial (exp2_poly_x2) instead of MUFU ex2:
 // the pairs i of each 32-column chunk with (i * N) % 16 < N, i.e. N of every 16
-// pairs spread evenly. Measured at N = 16384 (TFLOP/s for N = 0, 1, 2, 3, 4, 6):
-// d = 64 H = 48: 1105, 1105, 1085, 1003, 865, 861; d = 128 H = 24: 1764, 1779,
-// 1632 for N = 0, 1, 2. The softmax is not bound by the MUFU unit here (its
-// exponential phase is issue- and latency-bound, and the polynomial costs ten
-// instructions per pair against two MUFU issues), so no pair takes it.
+// pairs spread evenly. Measured at N = 16384 with a single MMA issuer (TFLOP/s
+// for N = 0, 1, 2, 3, 4, 6): d = 64 H = 48: 1105, 1105, 1085, 1003, 865, 861;
+// d = 128 H = 24: 1764, 1779, 1632 for N = 0, 1, 2. The exponential phase is
+// issue-bound, not MUFU-bound: an arithmetic-only test of it (two warps per SM
+// sub-partition, packed row sums) takes 39% and 60% more cycles per row with 2
+// and 4 of 16 pairs on the polynomial, which costs ten instructions per pair
+// against two MUFU issues. So no pair takes it.
 template <int D>
 struct PolyPairs {
   static constexpr int N = 0;
@@ -98,6 +106,16 @@ struct Cfg {
   static constexpr int SMEM = OFF_BAR + 512 + 1024;   // + slack to align the base to 1024
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
   static constexpr uint32_t COL_O0 = 256, COL_O1 = 256 + D;
+  // d = 64 leaves 128 Tensor Memory columns free, so P gets its own columns
+  // (bf16 pairs, 64 per tile) instead of overwriting S. S is then free once the
+  // softmax has read it, and the next QK^T of a tile is issued at that point,
+  // overlapping the tile's exponentials (EARLY_QK). At d = 128 S and O fill all
+  // 512 columns and P overwrites the S it came from.
+  static constexpr bool EARLY_QK = (D == 64);
+  static constexpr int THREADS = EARLY_QK ? 352 : 320;   // 8 softmax warps, issuer(s), loader
+  static constexpr uint32_t COL_P0 = EARLY_QK ? 256 + 2 * D : COL_S0;
+  static constexpr uint32_t COL_P1 = EARLY_QK ? 256 + 2 * D + 64 : COL_S1;
+  static_assert(!EARLY_QK || COL_P1 + 64 <= 512, "P columns past the Tensor Memory allocation");
 };
 
 // Store bookkeeping of one warp group, kept in shared memory and touched only by
@@ -112,6 +130,7 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[10], kv_empty[10];
   uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t s_free[2], pv_done[2];   // EARLY_QK only: S read by the softmax; PV(j) complete
   uint64_t wg_sync[2];
   uint64_t drain;
   StoreState store[2];  // per warp group
@@ -131,7 +150,7 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity,
                                              volatile int *abort_flag, uint64_t limit) {
   // The MMA issuer polls (it must react to a finished P at once); every other
   // role sleeps between polls so its waiting costs no issue slots.
-  const bool sleepy = (threadIdx.x / 32) != kMmaWarp;
+  const bool sleepy = (threadIdx.x / 32) != kMmaWarp && (threadIdx.x / 32) != kPvWarp;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (sleepy ? mbar_try_wait_sleep(bar, parity, kWaitSleepNs) : mbar_try_wait(bar, parity))
@@ -150,6 +169,24 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
                                            uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   return wait_phase_slow(bar, parity, abort_flag, limit);
+}
+
+// The same bounded wait with no out-of-line call, for a wait made while most
+// registers are live (a call there would force them to be spilled around it).
+__device__ __forceinline__ bool wait_phase_inline(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag, uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit) {
+        record_timeout(abort_flag);
+        return false;
+      }
+    }
+  }
 }
 
 // Wait used while tearing down after an abort: ignores the abort flag, still bounded.
@@ -381,11 +418,6 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
     for (int j = 1; j < nk; ++j) {
       const uint32_t sv = it % stages, sk = (it + 1) % stages;
       if (!wait(kv_full(sv), (it / stages) & 1)) goto drain;
-      // d = 64 (softmax-bound, MMA bursts half as long): K(j) is waited for with
-      // V(j-1), so nothing waits between a tile's PV and QK (+3% measured; at
-      // d = 128, K(j) is waited for only after PV0 is issued, which never
-      // depends on it).
-      if (D == 64 && !wait(kv_full(sk), ((it + 1) / stages) & 1)) goto drain;
       for (int t = 0; t < nt; ++t) {
         if (!wait(smem_u32(&bars->p_full[t]), pc[t] & 1)) goto drain;
         ++pc[t];
@@ -395,7 +427,8 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
           if (t == nt - 1) tc_commit(kv_empty(sv));   // V(j-1) is free once the last PV is done
         }
         __syncwarp();
-        if (D != 64 && t == 0) {
+        // K(j) is waited for only after PV0 is issued, which never depends on it.
+        if (t == 0) {
           if (!wait(kv_full(sk), ((it + 1) / stages) & 1)) goto drain;
           tc_fence_after();
         }
@@ -431,6 +464,122 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_
   }
 drain:
   // All MMAs this warp issued must finish before Tensor Memory is released.
+  if (elect_one()) tc_commit(smem_u32(&bars->drain));
+  __syncwarp();
+  drain_phase(smem_u32(&bars->drain), 0, lim);
+}
+
+// Issuers of the EARLY_QK schedule (d = 64). QK^T(j+1) of tile t goes into S_t
+// as soon as the softmax has read S(j) (s_free), so the next scores are computed
+// while the softmax works on the current ones; PV(j) of tile t reads P_t once
+// P(j) is written (p_full) and completes pv_done, which the softmax waits for
+// before it overwrites P_t or rescales O_t. QK^T and PV touch disjoint Tensor
+// Memory columns and have no order between them, so each has its own warp: an
+// issuing thread is held for about the run time of the MMAs it issues, and a
+// satisfied barrier wait costs ~150 cycles, so one thread doing both leaves the
+// tensor pipe idle during its waits; with two, one waits while the other's
+// MMAs run. A commit tracks only its own thread's MMAs, so each barrier below
+// is completed by the warp that issues the MMAs it stands for. The K/V ring
+// keeps the order K0 V0 K1 V1 ...: the QK warp consumes the even uses, the PV
+// warp the odd ones, each releasing its slot once both tiles' MMAs are done.
+template <int D, bool SHARED>
+__device__ void qk_issuer(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem_in,
+                          volatile int *abort_flag) {
+  using C = Cfg<D, SHARED>;
+  static_assert(C::EARLY_QK, "EARLY_QK schedule only");
+  const uint64_t lim = p.wait_limit_ns;
+  constexpr uint32_t stages = C::KV_STAGES;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_in, 0);
+  uint32_t base = 0, lu = 0;       // ring use of the unit's K0; items processed
+  uint32_t fc[2] = {0, 0};         // s_free phases waited for, per tile
+  bool used[2] = {false, false};   // S_t written before (its last scores must be read first)
+  const uint32_t q_full = smem_u32(&bars->q_full), q_empty = smem_u32(&bars->q_empty);
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, lim));
+  };
+  uint64_t qdesc[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    qdesc[t] = smem_desc_sw128(smem_u32(smem + C::OFF_Q + t * C::TILE), 16, 1024);
+  const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
+  auto kdesc = [&](uint32_t s) { return kdesc0 + static_cast<uint64_t>(s * (C::TILE >> 4)); };
+  const uint32_t col_s[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
+  Item item;
+  for (; get_item(p, static_cast<int>(lu), item); ++lu) {
+    const int nk = item.kv1 - item.kv0;
+    const int nt = unit_tiles(p, item.unit);
+    if (!wait(q_full, lu & 1)) goto drain;
+    for (int j = 0; j < nk; ++j) {
+      const uint32_t use = base + 2 * j, sk = use % stages;
+      if (!wait(smem_u32(&bars->kv_full[sk]), (use / stages) & 1)) goto drain;
+      for (int t = 0; t < nt; ++t) {
+        if (used[t]) {
+          if (!wait(smem_u32(&bars->s_free[t]), fc[t] & 1)) goto drain;
+          ++fc[t];
+        }
+        used[t] = true;
+        tc_fence_after();
+        if (elect_one()) {
+          issue_qk<D>(col_s[t], qdesc[t], kdesc(sk));
+          tc_commit(smem_u32(&bars->s_full[t]));
+          if (t == nt - 1) {
+            tc_commit(smem_u32(&bars->kv_empty[sk]));
+            if (j == nk - 1) tc_commit(q_empty);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    base += 2 * nk;
+  }
+drain:
+  // All MMAs this warp issued must finish before Tensor Memory is released.
+  if (elect_one()) tc_commit(smem_u32(&bars->drain));
+  __syncwarp();
+  drain_phase(smem_u32(&bars->drain), 0, lim);
+}
+
+template <int D, bool SHARED>
+__device__ void pv_issuer(const AttnParams &p, uint8_t *smem, Bars *bars, uint32_t tmem_in,
+                          volatile int *abort_flag) {
+  using C = Cfg<D, SHARED>;
+  static_assert(C::EARLY_QK, "EARLY_QK schedule only");
+  const uint64_t lim = p.wait_limit_ns;
+  constexpr uint32_t stages = C::KV_STAGES;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_in, 0);
+  uint32_t base = 0, lu = 0;
+  uint32_t pc[2] = {0, 0};
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, lim));
+  };
+  const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + C::OFF_KV), kHalfBytes, 1024);
+  auto vdesc = [&](uint32_t s) { return vdesc0 + static_cast<uint64_t>(s * (C::TILE >> 4)); };
+  const uint32_t col_o[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
+  const uint32_t col_p[2] = {tmem + C::COL_P0, tmem + C::COL_P1};
+  Item item;
+  for (; get_item(p, static_cast<int>(lu), item); ++lu) {
+    const int nk = item.kv1 - item.kv0;
+    const int nt = unit_tiles(p, item.unit);
+    for (int j = 0; j < nk; ++j) {
+      const bool last = j == nk - 1;
+      const uint32_t use = base + 2 * j + 1, sv = use % stages;
+      if (!wait(smem_u32(&bars->kv_full[sv]), (use / stages) & 1)) goto drain;
+      for (int t = 0; t < nt; ++t) {
+        if (!wait(smem_u32(&bars->p_full[t]), pc[t] & 1)) goto drain;
+        ++pc[t];
+        tc_fence_after();
+        if (elect_one()) {
+          issue_pv<D>(col_o[t], col_p[t], vdesc(sv), j > 0 ? 1u : 0u);
+          tc_commit(smem_u32(last ? &bars->o_full[t] : &bars->pv_done[t]));
+          if (t == nt - 1) tc_commit(smem_u32(&bars->kv_empty[sv]));
+          if (last && nt == 1) tc_commit(smem_u32(&bars->o_full[1]));   // group 1 sits this unit out
+        }
+        __syncwarp();
+      }
+    }
+    base += 2 * nk;
+  }
+drain:
   if (elect_one()) tc_commit(smem_u32(&bars->drain));
   __syncwarp();
   drain_phase(smem_u32(&bars->drain), 0, lim);
@@ -752,11 +901,13 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_base + (t == 0 ? C::COL_S0 : C::COL_S1);
   const uint32_t tO = tmem + lane_base + (t == 0 ? C::COL_O0 : C::COL_O1);
+  const uint32_t tP = tmem + lane_base + (t == 0 ? C::COL_P0 : C::COL_P1);
   const uint32_t s_full = smem_u32(&bars->s_full[t]), p_full = smem_u32(&bars->p_full[t]);
+  const uint32_t s_free = smem_u32(&bars->s_free[t]), pv_done = smem_u32(&bars->pv_done[t]);
   const uint32_t o_full = smem_u32(&bars->o_full[t]), wg_sync = smem_u32(&bars->wg_sync[t]);
   uint8_t *stg = smem + C::OFF_KV + (SHARED ? C::NREG - 1 : C::NREG - 2 + t) * C::TILE;
   const float scale = p.scale_log2;
-  uint32_t sc = 0, wgc = 0, lu = 0;
+  uint32_t sc = 0, wgc = 0, lu = 0, pvc = 0;
   StoreState &ss = bars->store[t];
   if (elected) ss = StoreState{0, 0, NSLAB, 0, 0};
 
@@ -791,6 +942,11 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
       row_max_part(s[0], s[1], mp, true);
       tmem_wait_ld_regs(s[2]);
       tmem_wait_ld_regs(s[3]);
+      if constexpr (C::EARLY_QK) {
+        // S is in registers: the issuer may compute the next scores into it.
+        tc_fence_before();
+        mbar_arrive(s_free);
+      }
       row_max_part(s[2], s[3], mp, false);
       const float mx = max3(max3(mp[0], mp[1], mp[2]), max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       const float m_new = fmaxf(m, mx * scale);
@@ -811,11 +967,18 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
         }
       }
       // p = 2^(s*scale - m): the argument on packed pairs, the row sum as four
-      // scalar chains (packing the two MUFU results for a packed add costs more
-      // registers than it saves), P as bf16 pairs over the S columns already read.
+      // scalar chains at d = 128 (there packing the two MUFU results for a packed
+      // add costs more registers than it saves) and as packed pairs at d = 64, P
+      // as bf16 pairs (over the S columns already read at d = 128).
       const float neg_m = -m;
       const uint64_t scale2 = f2_pack(scale, scale), negm2 = f2_pack(neg_m, neg_m);
       float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+      // With EARLY_QK (d = 64) the softmax is what bounds the kernel, and its
+      // exponential phase is issue-bound: the row sum runs as two packed fp32x2
+      // chains, one add per pair of columns instead of two (+7% measured at
+      // N = 16384; the scalar chains are kept at d = 128, where they cost no time).
+      constexpr bool PACKED_SUM = C::EARLY_QK;
+      uint64_t l2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -832,12 +995,33 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, Bars *bars, uin
             p0 = ex2_approx(x0);
             p1 = ex2_approx(x1);
           }
-          lsum[i & 3] += p0 + p1;
+          if constexpr (PACKED_SUM) {
+            l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
+          } else {
+            lsum[i & 3] += p0 + p1;
+          }
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tS + 16 * c, pk);
+        if constexpr (C::EARLY_QK) {
+          // P_t and O_t are read by PV(j-1) until pv_done completes: wait before
+          // the first store (holding more chunks of P back measured slower).
+          if (c == 0 && j > 0) {
+            ok = wait_phase_inline(pv_done, pvc & 1, abort_flag, lim);
+            ++pvc;
+            if (!__all_sync(0xffffffffu, ok)) goto teardown;
+            tc_fence_after();
+          }
+        }
+        tmem_st16((C::EARLY_QK ? tP : tS) + 16 * c, pk);
       }
-      l = fmaf(l, alpha, (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
+      if constexpr (PACKED_SUM) {
+        const uint64_t ls2 = f2_add(l2[0], l2[1]);
+        float a0, a1;
+        f2_unpack(ls2, a0, a1);
+        l = fmaf(l, alpha, a0 + a1);
+      } else {
+        l = fmaf(l, alpha, (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
+      }
       if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -943,7 +1127,8 @@ teardown:
 }
 
 template <int D, bool SHARED>
-__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__((Cfg<D, SHARED>::THREADS), 1)
+    attn_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D, SHARED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -962,9 +1147,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(smem_u32(&bars->s_full[t]), 1);
       mbar_init(smem_u32(&bars->p_full[t]), 128);
       mbar_init(smem_u32(&bars->o_full[t]), 1);
+      mbar_init(smem_u32(&bars->s_free[t]), 128);
+      mbar_init(smem_u32(&bars->pv_done[t]), 1);
       mbar_init(smem_u32(&bars->wg_sync[t]), 128);
     }
-    mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->drain), C::EARLY_QK ? 2 : 1);   // one commit per issuing warp
     bars->abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -987,7 +1174,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     load_role<D, SHARED>(p, smem, bars, abort_flag);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    mma_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
+    if constexpr (C::EARLY_QK)
+      qk_issuer<D, SHARED>(p, smem, bars, tmem, abort_flag);
+    else
+      mma_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    if constexpr (C::EARLY_QK) pv_issuer<D, SHARED>(p, smem, bars, tmem, abort_flag);
     __syncwarp();
   } else {
     softmax_role<D, SHARED>(p, smem, bars, tmem, abort_flag);
@@ -1076,7 +1269,7 @@ static cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, SHARED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_kernel<D, SHARED><<<grid, kThreads, smem, s>>>(p);
+  attn_kernel<D, SHARED><<<grid, Cfg<D, SHARED>::THREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 

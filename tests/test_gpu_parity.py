@@ -159,6 +159,10 @@ def test_identical_v_rows(xs):
     (1, 3, 640, 128, 5, 4.0),     # 5 tiles, peaked rows
     (1, 1, 128, 128, 1, 1.0),     # one tile, one KV step
     (3, 1, 256, 64, 8, 2.0),      # 32-row shards: a tile spans 4 shards
+    # d = 64 runs the early-QK schedule (separate P columns, QK and PV issuers):
+    (1, 2, 384, 64, 3, 1.0),      # odd tile count: group 1 sits the last unit out
+    (1, 1, 128, 64, 1, 1.0),      # one KV step: the issuers' first step is their last
+    (2, 2, 640, 64, 5, 4.0),      # 5 tiles, peaked rows (rescales between steps)
 ])
 def test_shapes_vs_oracle(xs, B, H, N, d, P, qs):
     q, k, v = inputs.qkv(B, N, H, d, seed=31 + N + P, q_scale=qs)
