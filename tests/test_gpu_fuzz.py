@@ -4,7 +4,11 @@ The shapes are drawn once from a fixed seed: B, H, N (a multiple of 128, odd
 tile counts included), d in {64, 128, 256}, P dividing N into 16-row-aligned
 shards, store_tile (8 only at d = 256), with or without a workspace (so some
 launches take the balanced schedule with units cut into pieces on several
-CTAs). Sizes stay small enough for the full oracle to finish in seconds."""
+CTAs). Sizes stay small enough for the full oracle to finish in seconds.
+XS_FUZZ_SHAPES and XS_FUZZ_SEED draw a longer or different list (default 28
+shapes from seed 2024)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -16,7 +20,8 @@ from gpu_util import assert_close, shards_bits, shards_f64
 pytestmark = pytest.mark.gpu
 
 
-def _shapes(n=28, seed=2024):
+def _shapes(n=int(os.environ.get("XS_FUZZ_SHAPES", "28")),
+            seed=int(os.environ.get("XS_FUZZ_SEED", "2024"))):
     rng = np.random.default_rng(seed)
     out = []
     while len(out) < n:
