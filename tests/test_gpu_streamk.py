@@ -272,3 +272,25 @@ def test_streamk_fused_ex_vs_oracle(xs, ws, st, flags):
                  f"fused_ex st={st} flags={flags}")
     t = spans.view(n_tiles, 2).cpu().numpy()
     assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])
+
+
+# (B, H, N, d, P): shapes that take the balanced schedule, one per kernel.
+@pytest.mark.parametrize("B,H,N,d,P", [(1, 2, 2944, 128, 4), (1, 1, 2816, 64, 4),
+                                       (1, 2, 2944, 256, 4)])
+def test_workspace_writes_stay_within_reported_bytes(xs, B, H, N, d, P):
+    """A workspace of exactly the bytes xs_workspace_bytes reports: the balanced
+    schedule's partial results and merge counters stay inside it (a canary
+    after it is untouched), and the output still matches the oracle."""
+    n, cut = xs.workspace_bytes(B, N, H, d)
+    assert cut == 1 and n > 0
+    canary = 1 << 20
+    buf = torch.full((n + canary,), 0xA5, dtype=torch.uint8, device="cuda")
+    q, k, v = inputs.qkv(B, N, H, d, seed=331 + N + d)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    xs.set_workspace(buf[:n])
+    try:
+        for st in ((8,) if d == 256 else (8, 2)):
+            assert_close(shards_f64(_fused(xs, q, k, v, P, st)), ref, f"d{d} st={st} exact workspace")
+    finally:
+        xs.set_workspace(None)
+    assert bool((buf[n:] == 0xA5).all()), "the balanced schedule wrote past its workspace"
