@@ -436,3 +436,32 @@ def test_concurrent_host_threads(xs):
     for (q, k, v, P, _, shards) in cases:
         assert_close(shards_f64(shards), oracle.shard_layout(oracle.attention(q, k, v), P),
                      "concurrent host threads")
+
+
+# ------------------------------------------------------------------ canaries
+
+@pytest.mark.parametrize("B,H,N,d,P", [(1, 3, 384, 64, 3), (2, 2, 512, 128, 8), (1, 2, 128, 128, 8),
+                                       (1, 2, 640, 256, 5)])
+def test_stores_stay_inside_the_destinations(xs, B, H, N, d, P):
+    """The P destinations carved from one allocation with 4 KiB canaries before,
+    between and after them: the fused stores fill every destination element and
+    touch no canary byte (16-row destinations and an odd tile count included)."""
+    R, gap = N // P, 4096 // 2                       # gap in bf16 elements
+    n_sh = B * R * H * d
+    total = gap + P * (n_sh + gap)
+    q, k, v = inputs.qkv(B, N, H, d, seed=337 + N + d)
+    ref = oracle.shard_layout(oracle.attention(q, k, v), P)
+    for st in ((8,) if d == 256 else (1, 8)):
+        buf = torch.full((total,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        canary = buf.view(torch.int16).clone()
+        shards = [buf[gap + p * (n_sh + gap): gap + p * (n_sh + gap) + n_sh].view(B, R, H, d)
+                  for p in range(P)]
+        xs.attn_fused(*_dev(q, k, v), shards, store_tile=st)
+        torch.cuda.synchronize()
+        assert xs.last_device_status() == xs.OK
+        bits = buf.view(torch.int16)
+        for p in range(P + 1):                        # the P + 1 canaries
+            lo = p * (n_sh + gap)
+            assert torch.equal(bits[lo:lo + gap], canary[lo:lo + gap]), f"st={st}: canary {p} written"
+        assert all(bool(torch.isfinite(s).all()) for s in shards), f"st={st}: element not written"
+        assert_close(shards_f64(shards), ref, f"st={st} carved destinations")
