@@ -294,3 +294,25 @@ def test_workspace_writes_stay_within_reported_bytes(xs, B, H, N, d, P):
     finally:
         xs.set_workspace(None)
     assert bool((buf[n:] == 0xA5).all()), "the balanced schedule wrote past its workspace"
+
+
+@pytest.mark.parametrize("H,d", [(4, 64), (2, 128), (2, 256)])
+def test_streamk_odd_tile_count_long_sampled(xs, H, d):
+    """N = 65408 (511 query tiles: the last unit of every head has a tile the second
+    group sits out) under the balanced schedule with the workspace the library
+    reports: sampled rows, the last rows of the sequence among them, against the
+    oracle, and every destination element written."""
+    B, N, P = 1, 65408, 8
+    assert _cut(xs, B, N, H, d) == 1
+    q, k, v = inputs.qkv(B, N, H, d, seed=347 + d)
+    buf = xs.alloc_workspace(B, N, H, d)
+    try:
+        shards = _fused(xs, q, k, v, P, 8)
+    finally:
+        xs.set_workspace(None)
+    del buf
+    assert all_finite_dev(shards)
+    rows = sample_rows(N, P, np.random.default_rng(347 + d), extra=12)
+    assert N - 1 in rows
+    assert_close(gather_rows_dev(shards, rows, N, P), oracle.attention_rows(q, k, v, rows),
+                 f"N65408 H{H} d{d} stream-K")
